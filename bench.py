@@ -1,0 +1,451 @@
+"""Benchmark of the expanded-layout MoE prefill layer on GB300.
+
+One step = one pass of the whole layer (layout, expand-scatter, gate_up GEMM,
+silu*mul + fp8 quant with the weight fold, down GEMM, combine) over one batch
+of the Zipf-routed T=16384, H=7168, I=2048, E=32, top-8 workload (the
+configuration the layer's targets are stated on), inputs resident in HBM.
+
+Prints one JSON line. ``value`` is whole-job tokens/s (valid tokens of all
+ranks / max-over-ranks time); ``roofline`` is for the dominant kernel (the
+gate_up GEMM) from CUDA events around its launches in the timed region;
+``e2e`` is the same metric through ExpandedMoELayer.forward with the inputs
+copied from pinned host memory and the output copied back every step;
+``cpu_baseline`` is the CPU oracle on a sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE prefill layer tokens/s; scatter+combine HBM GB/s; grouped FP8 TFLOP/s"
+WORKLOAD = synth.CONFIGS[2]          # zipf_t16384_h7168
+L2_FLUSH_BYTES = 256 << 20           # > the 126 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0                   # nominal dense fp8 : bf16 tensor rate
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD.name)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-sample-seconds", type=float, default=15.0)
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_config(cfg: synth.LayerConfig, rank: int) -> synth.LayerConfig:
+    """Weak scaling: every rank gets its own batch of the same shape."""
+    import dataclasses
+    return dataclasses.replace(cfg, seed=cfg.seed + 1000 * rank) if rank else cfg
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.device_index = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.device_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_work(cfg, P: int, M_pad: int, nv: int):
+    """Bytes or flops each step must move or compute (valid work only)."""
+    H, I, K = cfg.H, cfg.I, cfg.K
+    GH, GI = H // 128, I // 128
+    sbytes = 4 if cfg.scale_mode == "f32" else 1
+    M_cap_rows = M_pad
+    return {
+        "layout": 4 * cfg.T * K * 2 + 4 * M_cap_rows,
+        "scatter": nv * (H + GH * sbytes) + 4 * nv * K + M_pad * (H + GH * sbytes + 4),
+        "gemm1": 2.0 * P * (2 * I) * H,
+        "act_quant": M_pad * (2 * 2 * I + I + GI * sbytes),
+        "gemm2": 2.0 * P * H * I,
+        "combine": 2 * P * H + 2 * nv * H + 4 * nv * K,
+    }
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, world, rank, local):
+    import expanded_layout_expert_gb300 as mx
+    from expanded_layout_expert_gb300 import build as libbuild
+
+    libbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    init_dist(world, "nccl")
+    cfg = rank_config(synth.config_by_name(args.workload), rank)
+    d = synth.generate(cfg, device=dev)
+    nv = d["n_valid"]
+    n_valid = torch.tensor([nv], dtype=torch.int32, device=dev)
+    layer = mx.ExpandedMoELayer(d["w13"], d["s13"], d["w2"], d["s2"], K=cfg.K, align=cfg.align,
+                                scale_mode=cfg.scale_mode, max_tokens=cfg.T)
+    L = mx.load()
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    lay = layer.lay
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    x_q, x_s, ids, w = d["x_q"], d["x_s"], d["topk_ids"], d["topk_w"]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    names = ["layout", "scatter", "gemm1", "act_quant", "gemm2", "combine"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        mx.check(L.moe_expand_layout(ptr(ids), cfg.T, cfg.K, cfg.E, cfg.align, ptr(n_valid),
+                                     layer.M_cap, ptr(lay.psum), ptr(lay.start), ptr(lay.total),
+                                     ptr(lay.m_indices), ptr(lay.src2dst), ptr(lay.tile_prefix),
+                                     ptr(layer.ws), layer.ws.numel(), ptr(layer.status), s), "layout")
+        mark(1)
+        mx.check(L.moe_expand_scatter(ptr(x_q), ptr(x_s), layer.sl, x_s.shape[1], ptr(w),
+                                      ptr(lay.src2dst), ptr(lay.psum), ptr(lay.start), ptr(n_valid),
+                                      cfg.T, cfg.H, cfg.K, cfg.E, cfg.align, layer.M_cap,
+                                      ptr(layer.xe), ptr(layer.xe_scale), layer.xe_scale.shape[1],
+                                      ptr(layer.row_w), ptr(layer.status), s), "scatter")
+        mark(2)
+        mx.check(L.moe_grouped_gemm(ptr(layer.xe), ptr(layer.xe_scale), layer.sl,
+                                    layer.xe_scale.shape[1], ptr(lay.start), ptr(lay.tile_prefix),
+                                    ptr(lay.total), ptr(layer.w13), ptr(layer.s13), None, 0, cfg.E,
+                                    2 * cfg.I, cfg.H, layer.M_cap, ptr(layer.gateup),
+                                    ptr(layer.status), s), "gemm1")
+        mark(3)
+        fold = layer.flags & mx.MOE_FOLD_WEIGHT_INTO_SCALE
+        mx.check(L.moe_act_quant(ptr(layer.gateup), cfg.I, ptr(layer.row_w), fold, layer.sl,
+                                 ptr(lay.total), layer.M_cap, ptr(layer.down_in),
+                                 ptr(layer.down_in_scale), layer.down_in_scale.shape[1],
+                                 ptr(layer.status), s), "act_quant")
+        mark(4)
+        mx.check(L.moe_grouped_gemm(ptr(layer.down_in), ptr(layer.down_in_scale), layer.sl,
+                                    layer.down_in_scale.shape[1], ptr(lay.start),
+                                    ptr(lay.tile_prefix), ptr(lay.total), ptr(layer.w2),
+                                    ptr(layer.s2), ptr(layer.row_w),
+                                    layer.flags & mx.MOE_WEIGHT_OUTPUT_ROWS, cfg.E, cfg.H, cfg.I,
+                                    layer.M_cap, ptr(layer.down_out), ptr(layer.status), s), "gemm2")
+        mark(5)
+        mx.check(L.moe_combine(ptr(layer.down_out), ptr(lay.src2dst), None, ptr(n_valid), cfg.T,
+                               cfg.H, cfg.K, ptr(layer.y), s), "combine")
+        mark(6)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if layer.status.item() != 0:
+        raise RuntimeError(f"device status {layer.status.item()} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    with ClockSampler(local) as clocks:
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)          # evict the previous step's data from L2
+            step(evs[k])
+        torch.cuda.synchronize()
+    barrier(world)
+    t_wall = time.perf_counter() - t_wall0
+    per_kernel = {n: 0.0 for n in names}
+    step_ms = 0.0
+    for ev in evs:
+        for i, n in enumerate(names):
+            per_kernel[n] += ev[i].elapsed_time(ev[i + 1])
+        step_ms += ev[0].elapsed_time(ev[6])
+    step_ms /= args.steps
+    per_kernel = {n: v / args.steps for n, v in per_kernel.items()}
+    if layer.status.item() != 0:
+        raise RuntimeError(f"device status {layer.status.item()} in the timed region")
+
+    psum = lay.psum.cpu().numpy()
+    start = lay.start.cpu().numpy()
+    P = int((psum - start).sum())
+    M_pad = int(lay.total.item())
+    work = algorithmic_work(cfg, P, M_pad, nv)
+
+    step_ms_max = reduce_max(step_ms, world, dev)
+    tokens_all = reduce_sum(float(nv), world, dev)
+    value = tokens_all / (step_ms_max / 1e3)
+
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    fp8_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * FP8_PER_BF16
+    kernels = {}
+    for n in names:
+        ms = per_kernel[n]
+        if n.startswith("gemm"):
+            ach = work[n] / (ms / 1e3) / 1e12
+            kernels[n] = {"ms": round(ms, 4), "achieved": round(ach, 1), "unit": "TFLOP/s",
+                          "frac": round(ach / fp8_peak, 4), "work": work[n]}
+        else:
+            ach = work[n] / (ms / 1e3) / 1e9
+            kernels[n] = {"ms": round(ms, 4), "achieved": round(ach, 1), "unit": "GB/s",
+                          "frac": round(ach / hbm, 4), "work": work[n]}
+    sc_bytes = work["scatter"] + work["combine"]
+    sc_gbs = sc_bytes / ((per_kernel["scatter"] + per_kernel["combine"]) / 1e3) / 1e9
+    gemm_tflops = (work["gemm1"] + work["gemm2"]) / ((per_kernel["gemm1"] + per_kernel["gemm2"]) / 1e3) / 1e12
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3",
+        "data": "synthetic (seeded generator; no dataset or trained weights)",
+        "config": {"workload": cfg.name, "T": cfg.T, "n_valid": nv, "H": cfg.H, "I": cfg.I,
+                   "E": cfg.E, "top_k": cfg.K, "expert_alignment": cfg.align,
+                   "routing": f"zipf(s={cfg.zipf_s}), {cfg.zipf_zero_experts} experts empty",
+                   "inactive_rows": cfg.inactive_frac, "scales": cfg.scale_mode,
+                   "valid_pairs": P, "expanded_rows": M_pad, "M_cap": layer.M_cap,
+                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "parallelism": f"replicas x{world} (token-sharded, no collective)"},
+        "scatter_combine_gbs": round(sc_gbs, 1),
+        "grouped_fp8_tflops": round(gemm_tflops, 1),
+        "kernels": kernels,
+        "roofline": {"bound": "tensor", "kernel": "grouped_gemm (gate_up)",
+                     "achieved": kernels["gemm1"]["achieved"], "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": kernels["gemm1"]["frac"], "traffic": None,
+                     "peak_source": f"{peak_src}: bf16 burst x {FP8_PER_BF16:g} (nominal fp8:bf16)"},
+        "gpu_launches": mx.ExpandedMoELayer.KERNELS_PER_FORWARD * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, layer, d, dev, world)
+
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"], result["parity_sample"] = run_cpu_baseline(args, cfg, d, layer)
+    return result, rank
+
+
+def run_e2e(args, layer, d, dev, world):
+    """The same metric through ExpandedMoELayer.forward: inputs copied from
+    pinned host memory and the output copied back inside the timed region."""
+    host = {k: d[k].cpu().pin_memory() for k in ("x_q", "x_s", "topk_ids", "topk_w")}
+    nv_host = torch.tensor([d["n_valid"]], dtype=torch.int32).pin_memory()
+    dev_in = {k: torch.empty_like(d[k]) for k in host}
+    nv_dev = torch.empty(1, dtype=torch.int32, device=dev)
+    y_host = torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + 4
+    d2h = y_host.numel() * y_host.element_size()
+
+    def one():
+        for k, t in host.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        nv_dev.copy_(nv_host, non_blocking=True)
+        y = layer.forward(dev_in["x_q"], dev_in["x_s"], dev_in["topk_ids"], dev_in["topk_w"], nv_dev)
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    steps = max(5, args.steps // 2)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    ms = reduce_max(ms, world, dev)
+    tokens = reduce_sum(float(d["n_valid"]), world, dev)
+    return {"value": round(tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "api": "ExpandedMoELayer.forward with pinned host buffers"}
+
+
+def _oracle_sample(cfg, d, seconds: float, t_list=None):
+    """The CPU oracle's per-token path on valid tokens of the workload for about
+    `seconds`; returns (tokens, elapsed, {t: y_row})."""
+    import oracle
+    inp = oracle.to_numpy_inputs({k: v for k, v in d.items()})
+    nv = inp["n_valid"]
+    ids = inp["topk_ids"][:nv]
+    active = [int(t) for t in range(nv) if (ids[t] >= 0).any()]
+    order = t_list if t_list is not None else active[:: max(1, len(active) // 997)]
+    out = {}
+    t0 = time.perf_counter()
+    for t in order:
+        out[t] = oracle.token_forward(inp, t)
+        if time.perf_counter() - t0 > seconds:
+            break
+    return len(out), time.perf_counter() - t0, out
+
+
+def run_cpu_baseline(args, cfg, d, layer):
+    import numpy as np
+    n, secs, ys = _oracle_sample(cfg, d, args.cpu_sample_seconds)
+    ts = sorted(ys)
+    got = layer.y[ts].float().cpu().numpy().astype(np.float64)
+    want = np.stack([((ys[t].astype(np.uint32) << 16).view(np.float32)).astype(np.float64) for t in ts])
+    fro = float(np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-30))
+    mx = float(np.abs(got - want).max())
+    base = {"value": round(n / secs, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} valid tokens of {cfg.name} through the oracle's per-token path "
+                      f"(single-threaded C, fp64), {secs:.1f} s"}
+    return base, {"tokens": n, "rel_fro": fro, "max_abs": mx}
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None, rank
+    cfg = synth.config_by_name(args.workload)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    d = synth.generate(cfg, device=dev)
+    d = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    import oracle
+    inp = oracle.to_numpy_inputs(d)
+    nv = inp["n_valid"]
+    ids = inp["topk_ids"][:nv]
+    active = [int(t) for t in range(nv) if (ids[t] >= 0).any()]
+    stride = max(1, len(active) // (args.steps + args.warmup + 1))
+    tokens = active[::stride]
+    for i in range(args.warmup):
+        oracle.token_forward(inp, tokens[i % len(tokens)])
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.token_forward(inp, tokens[(args.warmup + i) % len(tokens)])
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = 1e3 / ms
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
+           "config": {"workload": cfg.name, "T": cfg.T, "n_valid": nv, "H": cfg.H, "I": cfg.I,
+                      "E": cfg.E, "top_k": cfg.K, "expert_alignment": cfg.align,
+                      "step": "one valid token through the oracle's per-token path"},
+           "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1,
+                            "kind": "oracle",
+                            "sample": f"{args.steps} valid tokens of {cfg.name}, one per step"},
+           "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    return res, rank
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        res, rank = run_reference(args, world, rank)
+    else:
+        res, rank = run_ours(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

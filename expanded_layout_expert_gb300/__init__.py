@@ -1,0 +1,269 @@
+"""Expanded-layout MoE prefill layer on GB300 (sm_103a).
+
+A thin binding over libmoe_expand.so (include/moe_expand.h): each function
+marshals torch tensors (device memory, owned by the caller) and the current
+CUDA stream into one C call; every step of the layer runs in the library's
+CUDA kernels. ``ExpandedMoELayer`` strings the calls together with buffers
+allocated once.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+
+from . import _capi
+from ._capi import (MOE_BLOCK_M, MOE_FOLD_WEIGHT_INTO_SCALE, MOE_GEMM_TILE_N128,
+                    MOE_SCALE_F32_ROWMAJOR, MOE_SCALE_UE8M0_PACKED_COLMAJOR,
+                    MOE_WEIGHT_OUTPUT_ROWS, MoEError, check, load)
+
+__all__ = [
+    "expanded_capacity", "workspace_size", "expand_layout", "expand_scatter", "grouped_gemm",
+    "act_quant", "grouped_ffn", "combine", "ExpandedMoELayer", "Layout", "MoEError",
+    "MOE_SCALE_F32_ROWMAJOR", "MOE_SCALE_UE8M0_PACKED_COLMAJOR", "MOE_FOLD_WEIGHT_INTO_SCALE",
+    "MOE_WEIGHT_OUTPUT_ROWS", "MOE_GEMM_TILE_N128", "MOE_BLOCK_M", "scale_layout_of",
+]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def scale_layout_of(mode: str) -> int:
+    return MOE_SCALE_UE8M0_PACKED_COLMAJOR if mode == "ue8m0" else MOE_SCALE_F32_ROWMAJOR
+
+
+def expanded_capacity(T: int, K: int, E: int, align: int) -> int:
+    return int(load().moe_expanded_capacity(T, K, E, align))
+
+
+def workspace_size(T: int, K: int, E: int) -> int:
+    return int(load().moe_workspace_size(T, K, E))
+
+
+@dataclasses.dataclass
+class Layout:
+    psum: torch.Tensor
+    start: torch.Tensor
+    total: torch.Tensor        # int32 [1], on the device
+    m_indices: torch.Tensor
+    src2dst: torch.Tensor
+    tile_prefix: torch.Tensor
+    E: int
+    align: int
+    M_cap: int
+
+
+def new_scale(rows: int, G: int, layout: int, device) -> torch.Tensor:
+    if layout == MOE_SCALE_F32_ROWMAJOR:
+        return torch.zeros(rows, G, dtype=torch.float32, device=device)
+    return torch.zeros((G + 3) // 4, rows, dtype=torch.int32, device=device)
+
+
+def scale_ld(s: torch.Tensor, layout: int) -> int:
+    return s.shape[1]
+
+
+def expand_layout(topk_ids: torch.Tensor, E: int, align: int, M_cap: int,
+                  n_valid: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                  status: Optional[torch.Tensor] = None, out: Optional[Layout] = None,
+                  stream=None) -> Layout:
+    T, K = topk_ids.shape
+    dev = topk_ids.device
+    if out is None:
+        out = Layout(psum=torch.empty(E, dtype=torch.int32, device=dev),
+                     start=torch.empty(E, dtype=torch.int32, device=dev),
+                     total=torch.empty(1, dtype=torch.int32, device=dev),
+                     m_indices=torch.empty(M_cap, dtype=torch.int32, device=dev),
+                     src2dst=torch.empty(T, K, dtype=torch.int32, device=dev),
+                     tile_prefix=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                     E=E, align=align, M_cap=M_cap)
+    if ws is None:
+        ws = torch.zeros(workspace_size(T, K, E), dtype=torch.uint8, device=dev)
+    rc = load().moe_expand_layout(_ptr(topk_ids), T, K, E, align, _ptr(n_valid), M_cap,
+                                  _ptr(out.psum), _ptr(out.start), _ptr(out.total),
+                                  _ptr(out.m_indices), _ptr(out.src2dst), _ptr(out.tile_prefix),
+                                  _ptr(ws), ws.numel(), _ptr(status), _stream(stream))
+    check(rc, "moe_expand_layout")
+    return out
+
+
+def expand_scatter(x_q: torch.Tensor, x_scale: torch.Tensor, scale_layout: int,
+                   topk_w: torch.Tensor, lay: Layout, n_valid: Optional[torch.Tensor] = None,
+                   xe: Optional[torch.Tensor] = None, xe_scale: Optional[torch.Tensor] = None,
+                   row_w: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                   stream=None):
+    T, H = x_q.shape
+    K = topk_w.shape[1]
+    dev = x_q.device
+    if xe is None:
+        xe = torch.zeros(lay.M_cap, H, dtype=torch.uint8, device=dev)
+    if xe_scale is None:
+        xe_scale = new_scale(lay.M_cap, H // 128, scale_layout, dev)
+    if row_w is None:
+        row_w = torch.zeros(lay.M_cap, dtype=torch.float32, device=dev)
+    rc = load().moe_expand_scatter(_ptr(x_q), _ptr(x_scale), scale_layout, x_scale.shape[1],
+                                   _ptr(topk_w), _ptr(lay.src2dst), _ptr(lay.psum),
+                                   _ptr(lay.start), _ptr(n_valid), T, H, K, lay.E, lay.align,
+                                   lay.M_cap, _ptr(xe), _ptr(xe_scale), xe_scale.shape[1],
+                                   _ptr(row_w), _ptr(status), _stream(stream))
+    check(rc, "moe_expand_scatter")
+    return xe, xe_scale, row_w
+
+
+def grouped_gemm(A: torch.Tensor, A_scale: torch.Tensor, scale_layout: int, lay: Layout,
+                 W: torch.Tensor, W_scale: torch.Tensor, row_w: Optional[torch.Tensor] = None,
+                 flags: int = 0, out: Optional[torch.Tensor] = None,
+                 status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    M_cap, Kd = A.shape
+    E, N, _ = W.shape
+    if out is None:
+        out = torch.zeros(M_cap, N, dtype=torch.bfloat16, device=A.device)
+    rc = load().moe_grouped_gemm(_ptr(A), _ptr(A_scale), scale_layout, A_scale.shape[1],
+                                 _ptr(lay.start), _ptr(lay.tile_prefix), _ptr(lay.total),
+                                 _ptr(W), _ptr(W_scale), _ptr(row_w), flags, E, N, Kd, M_cap,
+                                 _ptr(out), _ptr(status), _stream(stream))
+    check(rc, "moe_grouped_gemm")
+    return out
+
+
+def act_quant(gu: torch.Tensor, row_w: Optional[torch.Tensor], flags: int, scale_layout: int,
+              total: torch.Tensor, di: Optional[torch.Tensor] = None,
+              di_scale: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+              stream=None):
+    M_cap, twoI = gu.shape
+    I = twoI // 2
+    if di is None:
+        di = torch.zeros(M_cap, I, dtype=torch.uint8, device=gu.device)
+    if di_scale is None:
+        di_scale = new_scale(M_cap, I // 128, scale_layout, gu.device)
+    rc = load().moe_act_quant(_ptr(gu), I, _ptr(row_w), flags, scale_layout, _ptr(total), M_cap,
+                              _ptr(di), _ptr(di_scale), di_scale.shape[1], _ptr(status),
+                              _stream(stream))
+    check(rc, "moe_act_quant")
+    return di, di_scale
+
+
+def grouped_ffn(xe, xe_scale, scale_layout: int, lay: Layout, w13, s13, w2, s2, row_w, flags: int,
+                gateup=None, down_in=None, down_in_scale=None, down_out=None, status=None,
+                stream=None):
+    M_cap, H = xe.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    dev = xe.device
+    if gateup is None:
+        gateup = torch.zeros(M_cap, twoI, dtype=torch.bfloat16, device=dev)
+    if down_in is None:
+        down_in = torch.zeros(M_cap, I, dtype=torch.uint8, device=dev)
+    if down_in_scale is None:
+        down_in_scale = new_scale(M_cap, I // 128, scale_layout, dev)
+    if down_out is None:
+        down_out = torch.zeros(M_cap, H, dtype=torch.bfloat16, device=dev)
+    rc = load().moe_grouped_ffn(_ptr(xe), _ptr(xe_scale), xe_scale.shape[1], scale_layout,
+                                _ptr(lay.start), _ptr(lay.tile_prefix), _ptr(lay.total),
+                                _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), _ptr(row_w), flags,
+                                E, H, I, M_cap, _ptr(gateup), _ptr(down_in), _ptr(down_in_scale),
+                                down_in_scale.shape[1], _ptr(down_out), _ptr(status),
+                                _stream(stream))
+    check(rc, "moe_grouped_ffn")
+    return gateup, down_in, down_in_scale, down_out
+
+
+def combine(down: torch.Tensor, src2dst: torch.Tensor, row_w: Optional[torch.Tensor],
+            n_valid: Optional[torch.Tensor], out: torch.Tensor, stream=None) -> torch.Tensor:
+    T, K = src2dst.shape
+    H = down.shape[1]
+    rc = load().moe_combine(_ptr(down), _ptr(src2dst), _ptr(row_w), _ptr(n_valid), T, H, K,
+                            _ptr(out), _stream(stream))
+    check(rc, "moe_combine")
+    return out
+
+
+class ExpandedMoELayer:
+    """The whole expanded prefill layer for up to ``max_tokens`` token rows,
+    with every intermediate buffer allocated once.
+
+    forward(x_q, x_scale, topk_ids, topk_w, n_valid) -> y bf16 [T, H]
+      x_q      uint8 [T, H] fp8 e4m3 codes
+      x_scale  fp32 [T, H/128] (scale_mode "f32") or int32 [ceil(H/512), T]
+               packed ue8m0 exponents (scale_mode "ue8m0")
+      topk_ids int32 [T, K], -1 = no pair; topk_w fp32 [T, K]
+      n_valid  optional int32 [1] device tensor: rows >= n_valid are padding
+    On the fp32 path the top-k weight is folded into down_proj's input
+    scale; on the ue8m0 path it multiplies the down_proj output rows.
+    """
+
+    def __init__(self, w13, s13, w2, s2, *, K: int, align: int, scale_mode: str,
+                 max_tokens: int, device=None):
+        self.w13, self.s13, self.w2, self.s2 = w13, s13, w2, s2
+        self.E, twoI, self.H = w13.shape
+        self.I = twoI // 2
+        self.K, self.align = K, align
+        self.scale_mode = scale_mode
+        self.sl = scale_layout_of(scale_mode)
+        self.flags = MOE_WEIGHT_OUTPUT_ROWS if scale_mode == "ue8m0" else MOE_FOLD_WEIGHT_INTO_SCALE
+        self.T = max_tokens
+        dev = device if device is not None else w13.device
+        self.device = dev
+        self.M_cap = expanded_capacity(max_tokens, K, self.E, align)
+        E, H, I, M = self.E, self.H, self.I, self.M_cap
+        self.ws = torch.zeros(workspace_size(max_tokens, K, E), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.lay = Layout(psum=torch.zeros(E, dtype=torch.int32, device=dev),
+                          start=torch.zeros(E, dtype=torch.int32, device=dev),
+                          total=torch.zeros(1, dtype=torch.int32, device=dev),
+                          m_indices=torch.zeros(M, dtype=torch.int32, device=dev),
+                          src2dst=torch.zeros(max_tokens, K, dtype=torch.int32, device=dev),
+                          tile_prefix=torch.zeros(E + 1, dtype=torch.int32, device=dev),
+                          E=E, align=align, M_cap=M)
+        self.xe = torch.zeros(M, H, dtype=torch.uint8, device=dev)
+        self.xe_scale = new_scale(M, H // 128, self.sl, dev)
+        self.row_w = torch.zeros(M, dtype=torch.float32, device=dev)
+        self.gateup = torch.zeros(M, 2 * I, dtype=torch.bfloat16, device=dev)
+        self.down_in = torch.zeros(M, I, dtype=torch.uint8, device=dev)
+        self.down_in_scale = new_scale(M, I // 128, self.sl, dev)
+        self.down_out = torch.zeros(M, H, dtype=torch.bfloat16, device=dev)
+        self.y = torch.zeros(max_tokens, H, dtype=torch.bfloat16, device=dev)
+
+    def forward(self, x_q, x_scale, topk_ids, topk_w, n_valid=None, stream=None) -> torch.Tensor:
+        T = x_q.shape[0]
+        if T != self.T:
+            raise ValueError(f"layer was built for {self.T} token rows, got {T}")
+        L = load()
+        s = _stream(stream)
+        lay = self.lay
+        check(L.moe_expand_layout(_ptr(topk_ids), T, self.K, self.E, self.align, _ptr(n_valid),
+                                  self.M_cap, _ptr(lay.psum), _ptr(lay.start), _ptr(lay.total),
+                                  _ptr(lay.m_indices), _ptr(lay.src2dst), _ptr(lay.tile_prefix),
+                                  _ptr(self.ws), self.ws.numel(), _ptr(self.status), s),
+              "moe_expand_layout")
+        check(L.moe_expand_scatter(_ptr(x_q), _ptr(x_scale), self.sl, x_scale.shape[1],
+                                   _ptr(topk_w), _ptr(lay.src2dst), _ptr(lay.psum),
+                                   _ptr(lay.start), _ptr(n_valid), T, self.H, self.K, self.E,
+                                   self.align, self.M_cap, _ptr(self.xe), _ptr(self.xe_scale),
+                                   self.xe_scale.shape[1], _ptr(self.row_w), _ptr(self.status),
+                                   s), "moe_expand_scatter")
+        check(L.moe_grouped_ffn(_ptr(self.xe), _ptr(self.xe_scale), self.xe_scale.shape[1],
+                                self.sl, _ptr(lay.start), _ptr(lay.tile_prefix), _ptr(lay.total),
+                                _ptr(self.w13), _ptr(self.s13), _ptr(self.w2), _ptr(self.s2),
+                                _ptr(self.row_w), self.flags, self.E, self.H, self.I, self.M_cap,
+                                _ptr(self.gateup), _ptr(self.down_in), _ptr(self.down_in_scale),
+                                self.down_in_scale.shape[1], _ptr(self.down_out),
+                                _ptr(self.status), s), "moe_grouped_ffn")
+        check(L.moe_combine(_ptr(self.down_out), _ptr(lay.src2dst), None, _ptr(n_valid), T,
+                            self.H, self.K, _ptr(self.y), s), "moe_combine")
+        return self.y
+
+    # number of kernels one forward launches (layout 2, scatter 1, GEMM 2,
+    # act+quant 1, combine 1)
+    KERNELS_PER_FORWARD = 7

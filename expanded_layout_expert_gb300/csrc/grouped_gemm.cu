@@ -1,0 +1,426 @@
+// moe_grouped_gemm: FP8 block-scaled grouped GEMM over the expanded rows on
+// the 5th-generation tensor cores (the role of DeepGEMM's
+// grouped_gemm_nt_f8f8bf16_contig in SGLang moe_runner/deep_gemm.py,
+// _run_contiguous_gemm):
+//
+//   out[r, n] = bf16( sum_kb sA[r, kb] * sW[e, n/128, kb]
+//                            * sum_{k in block kb} A[r, k] * W[e, n, k] )
+//
+// for every row r of expert e's aligned segment. Activations carry one scale
+// per 1x128 group, weights one per 128x128 block.
+//
+// Design (one persistent CTA per SM, warp-specialised):
+//  - warp 0, one lane: TMA producer. Per 128-wide K block it loads the
+//    128-row A tile and the BN-row W tile (128-byte swizzle) into a ring of
+//    shared-memory stages.
+//  - warp 1, one lane: tcgen05.mma issuer (kind::f8f6f4, M=128, N=BN, K=32,
+//    4 instructions per K block). Each K block is accumulated into a fresh
+//    TMEM buffer (two buffers, ping-pong), because the fp32 block scales
+//    cannot be applied inside the tensor core.
+//  - warps 2..: epilogue. Each thread owns one row (its TMEM lane) and 128
+//    columns; per K block it reads the partial sums with tcgen05.ld and adds
+//    sA * sW * partial into fp32 registers ("promotion"), then frees the TMEM
+//    buffer. At the end of the tile it converts to bf16 and stores its row.
+// The m-tiles come from the layout's per-expert tile prefix, read on the
+// device: a CTA maps a linear tile id to (expert, m block, n block), and
+// tiles past the device-side total are never visited, so a capacity-sized
+// buffer costs nothing beyond its real rows.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "host_util.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;      // one scale block along K = one 128-byte swizzle row
+constexpr int UMMA_K = 32;   // K of one tcgen05.mma for 8-bit operands
+constexpr int kMaxE = 1024;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kABytes = BM * BK;
+  static constexpr int kBBytes = BN * BK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kEpiWarps = 4 * (BN / 128);
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem slot, abort flag
+  static constexpr int kTableOffset = kMiscOffset + 16;
+  static constexpr int kSmemBytes = 1024 + kTableOffset + (2 * kMaxE + 1) * 4;
+};
+
+struct Params {
+  const void* a_scale;
+  int64_t ld_as;
+  int ue8m0;
+  const void* w_scale;
+  const int32_t* start;
+  const int32_t* tile_prefix;
+  const int32_t* d_total;
+  const float* row_w;
+  int weight_rows;
+  int E, N, Kd;
+  int64_t M_cap;
+  uint16_t* out;
+  int32_t* status;
+};
+
+// Bounded wait used while draining: no abort check, only the time limit.
+MOE_DEV void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return;
+  }
+}
+
+MOE_DEV uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOffset);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOffset + 4);
+  int* s_tp = reinterpret_cast<int*>(smem + C::kTableOffset);
+  int* s_start = s_tp + (p.E + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], C::kEpiWarps);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_tp[i] = p.tile_prefix[i];
+  for (int i = threadIdx.x; i < p.E; i += blockDim.x) s_start[i] = p.start[i];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int total = *p.d_total;
+  if (total > p.M_cap) total = static_cast<int>(p.M_cap);
+  const int num_n = p.N / BN;
+  const int num_tiles = s_tp[p.E] * num_n;
+  const int KB = p.Kd / BK;
+  const int NB = p.N / 128;
+
+  // linear tile -> expert, first row, rows in this tile
+  auto tile_rows = [&](int tile, int& e, int& row0, int& rows) {
+    const int m = tile / num_n;
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_tp[mid] <= m) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    row0 = s_start[e] + (m - s_tp[e]) * BM;
+    const int seg_end = (e + 1 < p.E) ? min(s_start[e + 1], total) : total;
+    rows = min(BM, seg_end - row0);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        int e, row0, rows;
+        tile_rows(tile, e, row0, rows);
+        const int n0 = (tile % num_n) * BN;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          uint8_t* sa = smem + stage * C::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          tma_load_2d(sa, &tmA, kb * BK, row0, &full[stage]);
+          tma_load_2d(sa + C::kABytes, &tmB, kb * BK, e * p.N + n0, &full[stage]);
+          ++issued;
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      // Let the last loads land before the CTA can exit.
+      const int outstanding = issued < C::kStages ? issued : C::kStages;
+      for (int i = 1; i <= outstanding; ++i) {
+        int s = stage - i;
+        uint32_t ph = phase;
+        if (s < 0) { s += C::kStages; ph ^= 1u; }
+        drain_wait(&full[s], ph);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f8_f32(BM, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
+          const uint32_t sb = sa + C::kABytes;
+          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k)
+            tc_mma_f8(d, sw128_kmajor_desc(sa + k * UMMA_K), sw128_kmajor_desc(sb + k * UMMA_K),
+                      idesc, k > 0 ? 1u : 0u);
+          tc_commit(&empty[stage]);
+          tc_commit(&tfull[acc]);
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+        if (!ok) break;
+      }
+      // Every MMA issued so far must complete before TMEM is released.
+      tc_commit(mma_done);
+      drain_wait(mma_done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
+    const int half = ew >> 2;      // which 128-column half of the BN tile
+    const int row_in_tile = quarter * 32 + lane;
+    const uint8_t* ws8 = static_cast<const uint8_t*>(p.w_scale);
+    const float* wsf = static_cast<const float*>(p.w_scale);
+    int acc_buf = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int e, row0, rows;
+      tile_rows(tile, e, row0, rows);
+      const int n_tile = tile % num_n;
+      const int nb = (n_tile * BN) / 128 + half;
+      const int row = row0 + row_in_tile;
+      const bool row_ok = row_in_tile < rows && row < p.M_cap;
+      const int64_t wbase = (static_cast<int64_t>(e) * NB + nb) * KB;
+
+      auto scale_at = [&](int kb) -> float {
+        const float sw = p.ue8m0 ? ue8m0_to_f32(ws8[wbase + kb]) : wsf[wbase + kb];
+        float sa = 0.0f;
+        if (row_ok) {
+          if (p.ue8m0) {
+            const uint32_t word = static_cast<const uint32_t*>(
+                p.a_scale)[static_cast<int64_t>(kb >> 2) * p.ld_as + row];
+            sa = ue8m0_to_f32((word >> (8 * (kb & 3))) & 0xFFu);
+          } else {
+            sa = static_cast<const float*>(p.a_scale)[static_cast<int64_t>(row) * p.ld_as + kb];
+          }
+        }
+        return sa * sw;
+      };
+
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      float sc_next = scale_at(0);
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        const float sc = sc_next;
+        if (kb + 1 < KB) sc_next = scale_at(kb + 1);
+        // all lanes leave together: the TMEM loads below are warp-collective
+        const bool got = mbar_wait(&tfull[acc_buf], acc_phase, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(acc_buf * BN + half * 128);
+        if constexpr (BN == 256) {
+          // 16-column loads keep the staging registers small next to the
+          // 128 accumulators (10 warps leave 168 registers per thread).
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t v[16];
+            tc_ld16_wait(taddr + c * 16, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              acc[c * 16 + j] = fmaf(sc, __uint_as_float(v[j]), acc[c * 16 + j]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tc_ld32_wait(taddr + c * 32, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              acc[c * 32 + j] = fmaf(sc, __uint_as_float(v[j]), acc[c * 32 + j]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc_buf]);
+        acc_buf ^= 1;
+        if (acc_buf == 0) acc_phase ^= 1u;
+      }
+      if (!ok) break;
+      if (row_ok) {
+        const float wm = p.weight_rows ? p.row_w[row] : 1.0f;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.N +
+                                              n_tile * BN + half * 128);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          uint4 o;
+          o.x = pack_bf16x2(acc[v * 8 + 0] * wm, acc[v * 8 + 1] * wm);
+          o.y = pack_bf16x2(acc[v * 8 + 2] * wm, acc[v * 8 + 3] * wm);
+          o.z = pack_bf16x2(acc[v * 8 + 4] * wm, acc[v * 8 + 5] * wm);
+          o.w = pack_bf16x2(acc[v * 8 + 6] * wm, acc[v * 8 + 7] * wm);
+          dst[v] = o;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// 2-D uint8 tensor [outer, inner] with row stride `stride` bytes; box of
+// box_outer rows x 128 bytes, 128-byte swizzle, out-of-range rows read as 0.
+int make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t stride,
+              uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return MOE_ERR_CUDA;
+  }
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {stride};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+template <int BN>
+int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm, cudaStream_t s) {
+  using C = Cfg<BN>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return check_launch("cudaFuncSetAttribute(grouped_gemm_kernel)");
+    attr_set[dev] = true;
+  }
+  grouped_gemm_kernel<BN><<<device_sm_count(), C::kThreads, C::kSmemBytes, s>>>(ta, tb, prm);
+  return check_launch("grouped_gemm_kernel");
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale_layout,
+                                int64_t ld_as, const int32_t* start, const int32_t* tile_prefix,
+                                const int32_t* d_total, const uint8_t* W, const void* W_scale,
+                                const float* row_w, int flags, int E, int N, int Kd,
+                                int64_t M_cap, uint16_t* out, int32_t* d_status,
+                                moe_stream_t stream) {
+  MOE_REQUIRE(A && A_scale && start && tile_prefix && d_total && W && W_scale && out,
+              "moe_grouped_gemm: null pointer");
+  MOE_REQUIRE(E > 0 && E <= moe::kMaxE, "moe_grouped_gemm: E must be in [1, 1024]");
+  MOE_REQUIRE(N > 0 && N % 128 == 0 && Kd > 0 && Kd % 128 == 0,
+              "moe_grouped_gemm: N and Kd must be positive multiples of 128");
+  MOE_REQUIRE(M_cap > 0 && M_cap <= INT32_MAX && static_cast<int64_t>(E) * N <= INT32_MAX,
+              "moe_grouped_gemm: sizes exceed int32");
+  MOE_REQUIRE(scale_layout == MOE_SCALE_F32_ROWMAJOR || scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR,
+              "moe_grouped_gemm: bad scale layout");
+  if (scale_layout == MOE_SCALE_F32_ROWMAJOR) {
+    MOE_REQUIRE(ld_as >= Kd / 128, "moe_grouped_gemm: scale leading dimension < Kd/128");
+  } else {
+    MOE_REQUIRE(ld_as >= M_cap, "moe_grouped_gemm: packed scale leading dimension < M_cap");
+  }
+  MOE_REQUIRE(!(flags & MOE_WEIGHT_OUTPUT_ROWS) || row_w, "moe_grouped_gemm: row weighting needs row_w");
+  MOE_REQUIRE(moe::aligned(A, 16) && moe::aligned(W, 16) && moe::aligned(out, 16),
+              "moe_grouped_gemm: A, W and out must be 16-byte aligned");
+  MOE_REQUIRE_DEVICE();
+
+  const int BN = (N % 256 == 0 && !(flags & MOE_GEMM_TILE_N128)) ? 256 : 128;
+  CUtensorMap ta, tb;
+  int rc = moe::make_tmap(&ta, A, Kd, M_cap, Kd, moe::BM);
+  if (rc != MOE_OK) return rc;
+  rc = moe::make_tmap(&tb, W, Kd, static_cast<uint64_t>(E) * N, Kd, BN);
+  if (rc != MOE_OK) return rc;
+  moe::Params prm;
+  prm.a_scale = A_scale;
+  prm.ld_as = ld_as;
+  prm.ue8m0 = scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR;
+  prm.w_scale = W_scale;
+  prm.start = start;
+  prm.tile_prefix = tile_prefix;
+  prm.d_total = d_total;
+  prm.row_w = row_w;
+  prm.weight_rows = (flags & MOE_WEIGHT_OUTPUT_ROWS) ? 1 : 0;
+  prm.E = E;
+  prm.N = N;
+  prm.Kd = Kd;
+  prm.M_cap = M_cap;
+  prm.out = out;
+  prm.status = d_status;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return BN == 256 ? moe::launch<256>(ta, tb, prm, s) : moe::launch<128>(ta, tb, prm, s);
+}

@@ -1,0 +1,273 @@
+// moe_expand_layout: per-expert histogram, aligned prefix, row labels and
+// each pair's expanded row, computed on the device from topk_ids and the
+// device-side valid-row count (SGLang PR 37261, "feat(deepep_v2): expanded
+// (do_expand=True) prefill dispatch for DeepEP-V2": fill_m_indices_from_psum
+// labels rows from the device psum with no cumsum, no H2D copy and no
+// sentinel; the review thread fixes psum[i] = align(psum[i-1]) + count_i).
+//
+// Two launches, no spin-waits:
+//  1. count: each block histograms a 2048-pair chunk into the workspace; the
+//     last block to finish (atomic ticket, it never waits) scans the per-block
+//     counts into per-(expert, block) base rows and the per-expert aligned
+//     prefix, total and tile prefix.
+//  2. rank: each block re-reads its chunk in (token, k) order, warp by warp,
+//     and gives each valid pair base + rank (a stable counting sort); the
+//     same blocks label m_indices by binary search over the segment starts.
+#include "common.cuh"
+#include "host_util.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kPairsPerWarp = 256;
+constexpr int kChunk = kWarps * kPairsPerWarp;  // pairs per block
+constexpr int kMaxE = 1024;
+
+inline int64_t num_chunks(int64_t T, int K) {
+  const int64_t pairs = T * K;
+  const int64_t nb = (pairs + kChunk - 1) / kChunk;
+  return nb > 0 ? nb : 1;
+}
+
+MOE_DEV int64_t valid_rows(const int32_t* d_n_valid, int64_t T) {
+  if (d_n_valid == nullptr) return T;
+  const int64_t nv = *d_n_valid;
+  return nv < 0 ? 0 : (nv > T ? T : nv);
+}
+
+// Exclusive block-wide scan of one int per thread (kThreads threads).
+MOE_DEV int block_exclusive_scan(int v, int* warp_tot, int* block_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) base += warp_tot[w];
+    tot += warp_tot[w];
+  }
+  __syncthreads();
+  *block_total = tot;
+  return base + incl - v;
+}
+
+__global__ void __launch_bounds__(kThreads) layout_count_kernel(
+    const int32_t* __restrict__ ids, int64_t T, int K, int E, int align,
+    const int32_t* __restrict__ d_n_valid, int64_t M_cap, int nb, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offs, unsigned* __restrict__ ticket, int32_t* __restrict__ psum,
+    int32_t* __restrict__ start, int32_t* __restrict__ d_total, int32_t* __restrict__ tile_prefix,
+    int32_t* __restrict__ status) {
+  __shared__ int hist[kMaxE];
+  __shared__ int s_start[kMaxE];
+  __shared__ int warp_tot[kWarps];
+  __shared__ int s_last;
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += kThreads) hist[e] = 0;
+  __syncthreads();
+
+  const int64_t npairs = valid_rows(d_n_valid, T) * K;
+  const int64_t p0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+  for (int i = tid; i < kChunk; i += kThreads) {
+    const int64_t p = p0 + i;
+    if (p >= npairs) break;
+    const int id = ids[p];
+    if (id < 0) continue;
+    if (id >= E) {
+      set_status(status, MOE_ERR_DEVICE_CHECK);
+      continue;
+    }
+    atomicAdd(&hist[id], 1);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kThreads) counts[static_cast<int64_t>(e) * nb + blockIdx.x] = hist[e];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(ticket, 1u) == static_cast<unsigned>(nb - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // Last block. Per expert: exclusive scan over the blocks' counts.
+  const int lane = tid & 31, warp = tid >> 5;
+  for (int e = warp; e < E; e += kWarps) {
+    int carry = 0;
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+      const int b = b0 + lane;
+      const int c = (b < nb) ? __ldcg(&counts[static_cast<int64_t>(e) * nb + b]) : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (b < nb) offs[static_cast<int64_t>(e) * nb + b] = carry + incl - c;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) hist[e] = carry;  // count of expert e
+  }
+  __syncthreads();
+
+  // Over experts: start[e] = sum_{j<e} align(count_j), psum[e] = start[e] +
+  // count_e, tile prefix of ceil(align(count_e) / MOE_BLOCK_M).
+  const int per = (E + kThreads - 1) / kThreads;
+  const int e0 = tid * per;
+  int rows_local = 0, tiles_local = 0;
+  for (int j = 0; j < per; ++j) {
+    const int e = e0 + j;
+    if (e < E) {
+      const int seg = align_up(hist[e], align);
+      rows_local += seg;
+      tiles_local += (seg + MOE_BLOCK_M - 1) / MOE_BLOCK_M;
+    }
+  }
+  int rows_total, tiles_total;
+  int run = block_exclusive_scan(rows_local, warp_tot, &rows_total);
+  int trun = block_exclusive_scan(tiles_local, warp_tot, &tiles_total);
+  for (int j = 0; j < per; ++j) {
+    const int e = e0 + j;
+    if (e < E) {
+      const int c = hist[e];
+      const int seg = align_up(c, align);
+      start[e] = run;
+      s_start[e] = run;
+      psum[e] = run + c;
+      tile_prefix[e] = trun;
+      run += seg;
+      trun += (seg + MOE_BLOCK_M - 1) / MOE_BLOCK_M;
+    }
+  }
+  if (tid == 0) {
+    tile_prefix[E] = tiles_total;
+    *d_total = rows_total;
+    if (rows_total > M_cap) set_status(status, MOE_ERR_DEVICE_CHECK);
+  }
+  __syncthreads();
+  const int64_t n_offs = static_cast<int64_t>(E) * nb;
+  for (int64_t i = tid; i < n_offs; i += kThreads) offs[i] += s_start[i / nb];
+  if (tid == 0) *ticket = 0u;  // ready for the next call
+}
+
+__global__ void __launch_bounds__(kThreads) layout_rank_kernel(
+    const int32_t* __restrict__ ids, int64_t T, int K, int E, const int32_t* __restrict__ d_n_valid,
+    int64_t M_cap, int nb, const int32_t* __restrict__ offs, const int32_t* __restrict__ start,
+    const int32_t* __restrict__ d_total, int32_t* __restrict__ m_indices,
+    int32_t* __restrict__ src2dst) {
+  __shared__ int wcnt[kWarps * kMaxE];
+  __shared__ int s_start[kMaxE];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
+  for (int e = tid; e < E; e += kThreads) s_start[e] = start[e];
+  __syncthreads();
+
+  const int64_t all_pairs = T * K;
+  const int64_t npairs = valid_rows(d_n_valid, T) * K;
+  const int64_t base_p = static_cast<int64_t>(blockIdx.x) * kChunk + warp * kPairsPerWarp;
+  int* my = wcnt + warp * E;
+
+  // Pass 1: this warp's pairs per expert.
+  for (int r = 0; r < kPairsPerWarp; r += 32) {
+    const int64_t p = base_p + r + lane;
+    if (p < npairs) {
+      const int id = ids[p];
+      if (id >= 0 && id < E) atomicAdd(&my[id], 1);
+    }
+  }
+  __syncthreads();
+  // Pass 2: per expert, exclusive over the warps, on top of the block's base.
+  for (int e = tid; e < E; e += kThreads) {
+    int acc = offs[static_cast<int64_t>(e) * nb + blockIdx.x];
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  // Pass 3: in (token, k) order, 32 pairs at a time; lanes holding the same
+  // expert are ranked by lane, the lowest of them advances the counter.
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int r = 0; r < kPairsPerWarp; r += 32) {
+    const int64_t p = base_p + r + lane;
+    int id = -1;
+    bool valid = false;
+    if (p < npairs) {
+      id = ids[p];
+      valid = (id >= 0 && id < E);
+    }
+    const int key = valid ? id : (E + static_cast<int>(lane));
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    int dst = -1;
+    if (valid) dst = my[id] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (valid && (peers & lt_mask) == 0u) my[id] += __popc(peers);
+    __syncwarp();
+    if (p < all_pairs) src2dst[p] = (dst >= 0 && dst < M_cap) ? dst : -1;
+  }
+
+  // Row labels: e on [start[e], start[e] + align(count_e)), -1 past the total.
+  const int total = *d_total;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kThreads + tid; row < M_cap; row += stride) {
+    int label = -1;
+    if (row < total) {
+      int lo = 0, hi = E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_start[mid] <= row) lo = mid; else hi = mid - 1;
+      }
+      label = lo;
+    }
+    m_indices[row] = label;
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" size_t moe_workspace_size(int64_t T, int K, int E) {
+  if (T < 0 || K <= 0 || E <= 0) return 0;
+  const int64_t nb = moe::num_chunks(T, K);
+  const size_t tables = static_cast<size_t>(2) * static_cast<size_t>(E) * nb * sizeof(int32_t);
+  return (tables + 255) / 256 * 256 + 256;  // + the ticket, in its own 256-byte slot
+}
+
+extern "C" int moe_expand_layout(const int32_t* topk_ids, int64_t T, int K, int E, int align,
+                                 const int32_t* d_n_valid, int64_t M_cap, int32_t* psum,
+                                 int32_t* start, int32_t* d_total, int32_t* m_indices,
+                                 int32_t* src2dst, int32_t* tile_prefix, void* ws,
+                                 size_t ws_bytes, int32_t* d_status, moe_stream_t stream) {
+  MOE_REQUIRE(psum && start && d_total && tile_prefix, "moe_expand_layout: null output");
+  MOE_REQUIRE(T == 0 || (topk_ids && src2dst), "moe_expand_layout: null topk_ids/src2dst");
+  MOE_REQUIRE(M_cap == 0 || m_indices, "moe_expand_layout: null m_indices");
+  MOE_REQUIRE(T >= 0 && K > 0 && E > 0 && E <= moe::kMaxE && align > 0 && M_cap >= 0,
+              "moe_expand_layout: bad sizes T=%lld K=%d E=%d align=%d M_cap=%lld",
+              (long long)T, K, E, align, (long long)M_cap);
+  MOE_REQUIRE(T * K <= INT32_MAX && M_cap <= INT32_MAX, "moe_expand_layout: sizes exceed int32");
+  MOE_REQUIRE_DEVICE();
+  const size_t need = moe_workspace_size(T, K, E);
+  if (ws == nullptr || ws_bytes < need) {
+    moe::set_error("moe_expand_layout: workspace of %zu bytes needed", need);
+    return MOE_ERR_WORKSPACE;
+  }
+  const int nb = static_cast<int>(moe::num_chunks(T, K));
+  int32_t* counts = static_cast<int32_t*>(ws);
+  int32_t* offs = counts + static_cast<int64_t>(E) * nb;
+  unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + need - 256);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  moe::layout_count_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, align, d_n_valid, M_cap,
+                                                        nb, counts, offs, ticket, psum, start,
+                                                        d_total, tile_prefix, d_status);
+  int rc = moe::check_launch("layout_count_kernel");
+  if (rc != MOE_OK) return rc;
+  moe::layout_rank_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, d_n_valid, M_cap, nb,
+                                                       offs, start, d_total, m_indices, src2dst);
+  return moe::check_launch("layout_rank_kernel");
+}

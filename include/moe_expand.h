@@ -1,0 +1,203 @@
+/*
+ * moe_expand.h - C ABI of libmoe_expand.so, the expanded-layout MoE prefill
+ * layer for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (SGLang PR 37261, "feat(deepep_v2): expanded (do_expand=True)
+ * prefill dispatch for DeepEP-V2", Modifications/Core and the
+ * SGLANG_DEEPEP_V2_PREFILL_DO_EXPAND section; SGLang moe_runner/deep_gemm.py,
+ * _run_contiguous_gemm) on one GPU, with no all-to-all:
+ *
+ *   moe_expand_layout   per-expert histogram, aligned prefix (psum), row
+ *                       labels (m_indices), each pair's expanded row
+ *   moe_expand_scatter  one fp8 row per (token, expert) pair, grouped by
+ *                       expert, alignment gaps zeroed
+ *   moe_grouped_ffn     FP8 block-scaled grouped gate_up GEMM, silu*mul +
+ *                       per-128-group fp8 quant (top-k weight folded into the
+ *                       fp32 scale), grouped down GEMM
+ *   moe_combine         sum of each token's expert outputs back to [T, H] bf16
+ *
+ * Conventions for every call:
+ *  - All pointers named d_* or documented as "device" point to device memory
+ *    owned by the caller; the library allocates nothing and keeps no pointer
+ *    after a call returns. Host-only helpers say so.
+ *  - Calls are asynchronous on the given stream (NULL = legacy default
+ *    stream), do no host synchronisation and never read a device value on
+ *    the host: the valid-row count and the aligned total stay on the device
+ *    (vLLM PR 54109, "PaddedStandard activation format", Motivation: reading
+ *    the real/padding boundary on the host would break graph capture).
+ *  - The return value reports host-detectable errors (bad arguments, a
+ *    launch failure). Errors only the device can see (an expert id >= E in a
+ *    valid row, more expanded rows than M_cap, a bounded wait that gave up)
+ *    are written, first error wins, to the optional device word d_status
+ *    (int32, caller zeroes it); the kernel then skips the offending work and
+ *    returns instead of trapping.
+ *  - Row-major fp32 scales are [rows, ld] with ld >= G; packed ue8m0 scales
+ *    are int32 [ceil(G/4), ld] column-major with ld >= rows, four exponent
+ *    bytes per word, group 4j in the low byte, unused bytes zero (the layout
+ *    DeepGEMM's ue8m0 path reads; deep_gemm.py, pre_permute_deepep_v2_to_deep_gemm:
+ *    "packed UE8M0 scales require zero padding lanes").
+ *  - fp8 is OCP E4M3 stored as uint8; bf16 is stored as uint16.
+ */
+#ifndef MOE_EXPAND_H
+#define MOE_EXPAND_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* the same type as cudaStream_t */
+
+/* Return / status codes. */
+#define MOE_OK                0
+#define MOE_ERR_INVALID_ARG  -1  /* null pointer, bad shape or alignment */
+#define MOE_ERR_UNSUPPORTED  -2  /* device is not sm_103 */
+#define MOE_ERR_CUDA         -3  /* a CUDA call failed; see moe_last_error_string() */
+#define MOE_ERR_WORKSPACE    -4  /* workspace missing or too small */
+#define MOE_ERR_DEVICE_CHECK -5  /* device-detected: id >= E in a valid row, or total > M_cap */
+#define MOE_ERR_TIMEOUT      -6  /* device-detected: a bounded wait gave up */
+
+/* Scale layouts. */
+#define MOE_SCALE_F32_ROWMAJOR          0
+#define MOE_SCALE_UE8M0_PACKED_COLMAJOR 1
+
+/* moe_grouped_ffn / moe_grouped_gemm / moe_act_quant flags. */
+#define MOE_FOLD_WEIGHT_INTO_SCALE 1 /* fp32 path: store s*w as down_proj's input scale */
+#define MOE_WEIGHT_OUTPUT_ROWS     2 /* ue8m0 path: multiply the down_proj output row by w */
+#define MOE_GEMM_TILE_N128        16 /* tuning: use 128-column GEMM tiles even when N % 256 == 0 */
+
+/* Rows per grouped-GEMM tile; tile_prefix counts tiles of this height. */
+#define MOE_BLOCK_M 128
+
+/* Host. Upper bound on the expanded (aligned) row count over every routing
+ * of T*K assignments to E experts (deep_gemm.py, _get_compact_all_tokens):
+ * align * (min(A, E) + (A - min(A, E)) / align), A = T*K. Returns -1 on bad
+ * arguments. Size M_cap with it. */
+int64_t moe_expanded_capacity(int64_t T, int K, int E, int align);
+
+/* Host. Bytes of device workspace moe_expand_layout needs for (T, K, E).
+ * The workspace must be zero-filled once before its first use; every
+ * successful call leaves it ready for the next call. */
+size_t moe_workspace_size(int64_t T, int K, int E);
+
+/*
+ * Layout (SGLang PR 37261: fill_m_indices_from_psum; the review's
+ * definition psum[i] = align(psum[i-1]) + count_i; pre_permute_deepep_v2_to_deep_gemm).
+ *   topk_ids   device int32 [T, K]; -1 = no pair. Rows t >= *d_n_valid are
+ *              never read.
+ *   d_n_valid  device int32, rows [0, n_valid) are valid; NULL = all T.
+ *   align      expert_alignment (> 0).
+ *   M_cap      rows of the expanded buffers (m_indices length).
+ * Outputs (device, written every call):
+ *   psum       int32 [E]   inclusive aligned prefix: psum[e] = start[e] + count[e]
+ *   start      int32 [E]   start[e] = align(psum[e-1]), start[0] = 0
+ *   d_total    int32 [1]   align(psum[E-1]), a multiple of align
+ *   m_indices  int32 [M_cap]  e on [start[e], align(psum[e])), -1 on [total, M_cap)
+ *   src2dst    int32 [T, K]   expanded row of each valid pair, -1 otherwise;
+ *                             pairs of one expert are in ascending (t, k) order
+ *   tile_prefix int32 [E+1]   tile_prefix[e+1] - tile_prefix[e] =
+ *                             ceil((align(psum[e]) - start[e]) / MOE_BLOCK_M)
+ *   ws, ws_bytes  workspace of moe_workspace_size(T, K, E) bytes.
+ * Device errors: MOE_ERR_DEVICE_CHECK for an id >= E in a valid row (that
+ * pair is skipped) or total > M_cap (rows past M_cap are not written).
+ */
+int moe_expand_layout(const int32_t* topk_ids, int64_t T, int K, int E, int align,
+                      const int32_t* d_n_valid, int64_t M_cap,
+                      int32_t* psum, int32_t* start, int32_t* d_total,
+                      int32_t* m_indices, int32_t* src2dst, int32_t* tile_prefix,
+                      void* ws, size_t ws_bytes, int32_t* d_status, moe_stream_t stream);
+
+/*
+ * Expand-scatter (SGLang PR 37261, do_expand=True: per-(token, expert) rows
+ * grouped by expert; the copy ep_scatter_2 made before; vLLM PR 54109:
+ * alignment gaps are zeroed).
+ *   x          device uint8 [T, H] fp8 rows (H % 128 == 0, H <= 16384)
+ *   x_scale    device, scale_layout: fp32 [T, ld_xs] or packed ue8m0 [ceil(H/512), ld_xs]
+ *   topk_w     device fp32 [T, K]
+ *   src2dst, psum, start: from moe_expand_layout with the same align
+ * Outputs (device): xe uint8 [M_cap, H], xe_scale in the same layout family
+ * with leading dimension ld_xes, row_w fp32 [M_cap] (the pair's top-k
+ * weight). Row src2dst[t,k] = token t's bytes, scales and weight; rows
+ * [psum[e], align(psum[e])) are zero. Rows >= total are not written.
+ */
+int moe_expand_scatter(const uint8_t* x, const void* x_scale, int scale_layout, int64_t ld_xs,
+                       const float* topk_w, const int32_t* src2dst,
+                       const int32_t* psum, const int32_t* start, const int32_t* d_n_valid,
+                       int64_t T, int H, int K, int E, int align, int64_t M_cap,
+                       uint8_t* xe, void* xe_scale, int64_t ld_xes, float* row_w,
+                       int32_t* d_status, moe_stream_t stream);
+
+/*
+ * One block-scaled FP8 grouped GEMM over the expanded rows (DeepGEMM's
+ * grouped_gemm_nt_f8f8bf16_contig as _run_contiguous_gemm calls it):
+ *   out[r, n] = bf16( sum_kb sA[r, kb] * sW[e, n/128, kb] * sum_{k in kb} A[r,k] W[e,n,k] )
+ * for r in expert e's aligned segment, r < *d_total; other rows untouched.
+ *   A        device uint8 [M_cap, Kd], K-major, 16-byte aligned
+ *   A_scale  device, scale_layout, leading dimension ld_as
+ *   W        device uint8 [E, N, Kd] K-major ("nt"); W_scale fp32 [E, N/128, Kd/128]
+ *            (scale_layout F32) or uint8 ue8m0 bytes (scale_layout UE8M0)
+ *   start, tile_prefix, d_total: from moe_expand_layout
+ *   row_w    device fp32 [M_cap], read only with MOE_WEIGHT_OUTPUT_ROWS
+ *   out      device bf16 [M_cap, N]
+ * Needs N % 128 == 0, Kd % 128 == 0, E <= 1024.
+ */
+int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale_layout, int64_t ld_as,
+                     const int32_t* start, const int32_t* tile_prefix, const int32_t* d_total,
+                     const uint8_t* W, const void* W_scale, const float* row_w, int flags,
+                     int E, int N, int Kd, int64_t M_cap, uint16_t* out,
+                     int32_t* d_status, moe_stream_t stream);
+
+/*
+ * silu(g)*u and per-token-group fp8 quantisation (deep_gemm.py,
+ * _run_contiguous_gemm: silu_and_mul then per_token_group_quant with group
+ * 128; gate = columns [0, I), up = [I, 2I)). Per 128-group of h (h rounded to
+ * bf16): amax = max(max|h|, 1e-10), s = amax/448, q = e4m3_rn_sat(h/s).
+ * fp32 layout: stored scale s*row_w[r] with MOE_FOLD_WEIGHT_INTO_SCALE (the
+ * fold of SGLang PR 37261), else s. ue8m0 layout: s rounded up to a power of
+ * two (_cast_to_e8m0_with_rounding_up), stored as its exponent byte.
+ *   gu       device bf16 [M_cap, 2I]; rows r < *d_total are processed
+ *   di       device uint8 [M_cap, I]; di_scale in scale_layout with ld_ds
+ */
+int moe_act_quant(const uint16_t* gu, int I, const float* row_w, int flags, int scale_layout,
+                  const int32_t* d_total, int64_t M_cap, uint8_t* di, void* di_scale,
+                  int64_t ld_ds, int32_t* d_status, moe_stream_t stream);
+
+/*
+ * The expert FFN over the expanded rows: moe_grouped_gemm with W13 [E, 2I, H]
+ * into gateup_ws bf16 [M_cap, 2I], moe_act_quant into down_in uint8
+ * [M_cap, I] / down_in_scale (ld_dis), moe_grouped_gemm with W2 [E, H, I]
+ * into down_out bf16 [M_cap, H].
+ * flags: MOE_FOLD_WEIGHT_INTO_SCALE (fp32 scales) or MOE_WEIGHT_OUTPUT_ROWS
+ * (ue8m0 scales; a power-of-two scale cannot absorb the weight, so the output
+ * row is weighted instead), or 0 (unweighted; moe_combine may weight).
+ */
+int moe_grouped_ffn(const uint8_t* xe, const void* xe_scale, int64_t ld_xes, int scale_layout,
+                    const int32_t* start, const int32_t* tile_prefix, const int32_t* d_total,
+                    const uint8_t* w13, const void* s13, const uint8_t* w2, const void* s2,
+                    const float* row_w, int flags, int E, int H, int I, int64_t M_cap,
+                    uint16_t* gateup_ws, uint8_t* down_in, void* down_in_scale, int64_t ld_dis,
+                    uint16_t* down_out, int32_t* d_status, moe_stream_t stream);
+
+/*
+ * Combine (the expand-mode combine's un-expand and reduction; ep_gather):
+ *   y[t, :] = bf16( sum_{k: src2dst[t,k] >= 0} f32(down_out[src2dst[t,k], :]) * (row_w ? row_w[row] : 1) )
+ * for t < *d_n_valid, summed in k order in fp32. A token with no pair gets
+ * zeros; rows t >= n_valid are not written.
+ *   down_out device bf16 [M_cap, H] (H % 8 == 0); y device bf16 [T, H].
+ */
+int moe_combine(const uint16_t* down_out, const int32_t* src2dst, const float* row_w,
+                const int32_t* d_n_valid, int64_t T, int H, int K, uint16_t* y,
+                moe_stream_t stream);
+
+/* Host. Text of the last error raised on this thread (never NULL). */
+const char* moe_last_error_string(void);
+
+/* Host. 1 when `device` can run this library (compute capability 10.3). */
+int moe_device_supported(int device);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_EXPAND_H */
