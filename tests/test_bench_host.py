@@ -1,0 +1,67 @@
+"""Host logic of bench.py that needs no GPU: the N>1 aggregation (max of the
+step time over ranks, sum of tokens over ranks) on two gloo ranks, the
+per-rank workload seeds of the weak-scaling run, and the algorithmic work
+counts."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import synth
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    bench.init_dist(world, "gloo")
+    w, r, _ = bench.dist_env()
+    step_ms = 10.0 + 5.0 * r            # rank 1 is the slow one
+    mx = bench.reduce_max(step_ms, w, "cpu")
+    tok = bench.reduce_sum(1000.0 + r, w, "cpu")
+    cfg = bench.rank_config(synth.CONFIGS[1], r)
+    bench.barrier(w)
+    q.put((r, mx, tok, cfg.seed))
+    torch.distributed.destroy_process_group()
+
+
+def test_two_gloo_ranks_aggregate():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [o[1] for o in out] == [15.0, 15.0]
+    assert [o[2] for o in out] == [2001.0, 2001.0]
+    assert out[0][3] != out[1][3], "each rank draws its own batch"
+
+
+def test_algorithmic_work_counts():
+    import bench
+    cfg = synth.CONFIGS[2]
+    w = bench.algorithmic_work(cfg, P=1000, M_pad=1280, nv=130)
+    H, I = cfg.H, cfg.I
+    assert w["gemm1"] == 2.0 * 1000 * 2 * I * H
+    assert w["gemm2"] == 2.0 * 1000 * H * I
+    assert w["combine"] == 2 * 1000 * H + 2 * 130 * H + 4 * 130 * cfg.K
+    assert w["scatter"] == 130 * (H + (H // 128) * 4) + 4 * 130 * cfg.K + 1280 * (H + (H // 128) * 4 + 4)
+    assert w["act_quant"] == 1280 * (4 * I + I + (I // 128) * 4)
+
+
+def test_reference_arm_other_ranks_do_nothing():
+    import bench
+    res, rank = bench.run_reference(bench.parse_args(["--impl", "reference"]), 2, 1)
+    assert res is None and rank == 1
