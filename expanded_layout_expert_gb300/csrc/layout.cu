@@ -13,6 +13,8 @@
 //  2. rank: each block re-reads its chunk in (token, k) order, warp by warp,
 //     and gives each valid pair base + rank (a stable counting sort); the
 //     same blocks label m_indices by binary search over the segment starts.
+#include <mutex>
+
 #include "common.cuh"
 #include "host_util.h"
 
@@ -266,6 +268,102 @@ extern "C" int moe_expand_layout(const int32_t* topk_ids, int64_t T, int K, int 
                                                         nb, counts, offs, ticket, psum, start,
                                                         d_total, tile_prefix, d_status);
   int rc = moe::check_launch("layout_count_kernel");
+  if (rc != MOE_OK) return rc;
+  moe::layout_rank_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, d_n_valid, M_cap, nb,
+                                                       offs, start, d_total, m_indices, src2dst);
+  return moe::check_launch("layout_rank_kernel");
+}
+
+// ---------------------------------------------------------------------------
+// moe_expand_layout_noalloc: the same two kernels, with their scratch in a
+// fixed array that lives in the library's device image, so the caller passes
+// no workspace and nothing is allocated on this path. Meant for callers that
+// cannot allocate device memory at this point: a serving engine that has
+// already handed all of HBM to its own pool, or a host loop that must not
+// call cudaMalloc here because cudaMalloc can synchronise the device.
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB per device
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device. In host
+// code the array's name is only a host-side stand-in, never the device
+// address, so kernels must be given this pointer instead.
+void* g_noalloc_addr[64] = {};
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error("moe_expand_layout_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) {
+    set_error("moe_expand_layout_noalloc: device index %d out of range", dev);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      set_error("moe_expand_layout_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      return MOE_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" size_t moe_expand_layout_noalloc_max_scratch(void) { return moe::kNoAllocScratchBytes; }
+
+extern "C" int moe_expand_layout_noalloc(const int32_t* topk_ids, int64_t T, int K, int E,
+                                         int align, const int32_t* d_n_valid, int64_t M_cap,
+                                         int32_t* psum, int32_t* start, int32_t* d_total,
+                                         int32_t* m_indices, int32_t* src2dst,
+                                         int32_t* tile_prefix, int32_t* d_status,
+                                         moe_stream_t stream) {
+  MOE_REQUIRE(psum && start && d_total && tile_prefix, "moe_expand_layout_noalloc: null output");
+  MOE_REQUIRE(T == 0 || (topk_ids && src2dst), "moe_expand_layout_noalloc: null topk_ids/src2dst");
+  MOE_REQUIRE(M_cap == 0 || m_indices, "moe_expand_layout_noalloc: null m_indices");
+  MOE_REQUIRE(T >= 0 && K > 0 && E > 0 && E <= moe::kMaxE && align > 0 && M_cap >= 0,
+              "moe_expand_layout_noalloc: bad sizes T=%lld K=%d E=%d align=%d M_cap=%lld",
+              (long long)T, K, E, align, (long long)M_cap);
+  MOE_REQUIRE(T * K <= INT32_MAX && M_cap <= INT32_MAX,
+              "moe_expand_layout_noalloc: sizes exceed int32");
+  const size_t need = moe_workspace_size(T, K, E);
+  MOE_REQUIRE(need <= moe::kNoAllocScratchBytes,
+              "moe_expand_layout_noalloc: T=%lld K=%d E=%d needs %zu bytes of scratch, more than "
+              "the fixed %zu; use moe_expand_layout with a workspace",
+              (long long)T, K, E, need, moe::kNoAllocScratchBytes);
+  MOE_REQUIRE_DEVICE();
+  void* ws = nullptr;
+  int rc = moe::noalloc_scratch(&ws);
+  if (rc != MOE_OK) return rc;
+  const int nb = static_cast<int>(moe::num_chunks(T, K));
+  int32_t* counts = static_cast<int32_t*>(ws);
+  int32_t* offs = counts + static_cast<int64_t>(E) * nb;
+  unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + need - 256);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The array keeps whatever the previous call left; the ticket must start
+  // at zero (the counts and offsets are fully rewritten every call).
+  cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) {
+    moe::set_error("moe_expand_layout_noalloc: cudaMemsetAsync: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  moe::layout_count_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, align, d_n_valid, M_cap,
+                                                        nb, counts, offs, ticket, psum, start,
+                                                        d_total, tile_prefix, d_status);
+  rc = moe::check_launch("layout_count_kernel");
   if (rc != MOE_OK) return rc;
   moe::layout_rank_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, d_n_valid, M_cap, nb,
                                                        offs, start, d_total, m_indices, src2dst);

@@ -110,6 +110,37 @@ int moe_expand_layout(const int32_t* topk_ids, int64_t T, int K, int E, int alig
                       void* ws, size_t ws_bytes, int32_t* d_status, moe_stream_t stream);
 
 /*
+ * moe_expand_layout without a workspace argument. The pages have no
+ * counterpart of this call; it exists for callers that cannot allocate
+ * device memory when the layer runs - for example a serving engine that has
+ * handed nearly all of HBM to its own pool up front, or a host loop that
+ * must not call cudaMalloc on this path because cudaMalloc can synchronise
+ * the device. Arguments and outputs are those of moe_expand_layout.
+ *  - Scratch: a fixed 1 MiB array in the library's device image, held by
+ *    every GPU that loads the library until the process exits. A call needs
+ *    moe_workspace_size(T, K, E) bytes of it (2*E*ceil(T*K/2048)*4 bytes
+ *    rounded up to 256, plus 256: E = 32 fits up to 8.3 M (token, expert)
+ *    pairs, E = 1024 up to 258 k); larger sizes are rejected with
+ *    MOE_ERR_INVALID_ARG and a message, before any device work.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array and it keeps the last call's contents;
+ *    the call clears the part that must start at zero (an asynchronous 4-byte
+ *    memset on the stream). Calls that overlap on the GPU (different streams,
+ *    no ordering between them) race on the array and give wrong results.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+int moe_expand_layout_noalloc(const int32_t* topk_ids, int64_t T, int K, int E, int align,
+                              const int32_t* d_n_valid, int64_t M_cap,
+                              int32_t* psum, int32_t* start, int32_t* d_total,
+                              int32_t* m_indices, int32_t* src2dst, int32_t* tile_prefix,
+                              int32_t* d_status, moe_stream_t stream);
+
+/* Host. Bytes of the fixed scratch array moe_expand_layout_noalloc uses. */
+size_t moe_expand_layout_noalloc_max_scratch(void);
+
+/*
  * Expand-scatter (SGLang PR 37261, do_expand=True: per-(token, expert) rows
  * grouped by expert; the copy ep_scatter_2 made before; vLLM PR 54109:
  * alignment gaps are zeroed).
