@@ -49,6 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-seconds", type=float, default=15.0)
+    ap.add_argument("--gemm-tile-n128", action="store_true",
+                    help="force 128-column GEMM tiles (tuning comparison)")
     return ap.parse_args(argv)
 
 
@@ -197,6 +199,7 @@ def run_ours(args, world, rank, local):
     x_q, x_s, ids, w = d["x_q"], d["x_s"], d["topk_ids"], d["topk_w"]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     names = ["layout", "scatter", "gemm1", "act_quant", "gemm2", "combine"]
+    gflags = mx.MOE_GEMM_TILE_N128 if args.gemm_tile_n128 else 0
 
     def step(ev=None):
         def mark(i):
@@ -216,7 +219,7 @@ def run_ours(args, world, rank, local):
         mark(2)
         mx.check(L.moe_grouped_gemm(ptr(layer.xe), ptr(layer.xe_scale), layer.sl,
                                     layer.xe_scale.shape[1], ptr(lay.start), ptr(lay.tile_prefix),
-                                    ptr(lay.total), ptr(layer.w13), ptr(layer.s13), None, 0, cfg.E,
+                                    ptr(lay.total), ptr(layer.w13), ptr(layer.s13), None, gflags, cfg.E,
                                     2 * cfg.I, cfg.H, layer.M_cap, ptr(layer.gateup),
                                     ptr(layer.status), s), "gemm1")
         mark(3)
@@ -230,7 +233,7 @@ def run_ours(args, world, rank, local):
                                     layer.down_in_scale.shape[1], ptr(lay.start),
                                     ptr(lay.tile_prefix), ptr(lay.total), ptr(layer.w2),
                                     ptr(layer.s2), ptr(layer.row_w),
-                                    layer.flags & mx.MOE_WEIGHT_OUTPUT_ROWS, cfg.E, cfg.H, cfg.I,
+                                    (layer.flags & mx.MOE_WEIGHT_OUTPUT_ROWS) | gflags, cfg.E, cfg.H, cfg.I,
                                     layer.M_cap, ptr(layer.down_out), ptr(layer.status), s), "gemm2")
         mark(5)
         mx.check(L.moe_combine(ptr(layer.down_out), ptr(lay.src2dst), None, ptr(n_valid), cfg.T,

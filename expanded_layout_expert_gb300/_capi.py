@@ -52,6 +52,7 @@ SIGNATURES = {
     "moe_grouped_ffn": (I32, [P, P, I64, I32, P, P, P, P, P, P, P, P, I32, I32, I32, I32, I64,
                               P, P, P, I64, P, P, P]),
     "moe_combine": (I32, [P, P, P, P, I64, I32, I32, P, P]),
+    "moe_gemm_set_trace": (I32, [P]),
     "moe_last_error_string": (C.c_char_p, []),
     "moe_device_supported": (I32, [I32]),
 }

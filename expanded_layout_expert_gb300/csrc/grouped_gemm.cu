@@ -17,18 +17,27 @@
 //    4 instructions per K block). Each K block is accumulated into a fresh
 //    TMEM buffer (two buffers, ping-pong), because the fp32 block scales
 //    cannot be applied inside the tensor core.
-//  - warps 2..: epilogue. Each thread owns one row (its TMEM lane) and 128
-//    columns; per K block it reads the partial sums with tcgen05.ld and adds
-//    sA * sW * partial into fp32 registers ("promotion"), then frees the TMEM
-//    buffer. At the end of the tile it converts to bf16 and stores its row.
+//  - warps 2..: epilogue (four warps per 128 columns of the tile). Each
+//    thread owns one row (its TMEM lane) and 128 columns; per K block it
+//    reads the partial sums with tcgen05.ld and adds sA * sW * partial into
+//    fp32 registers with packed fma.rn.f32x2 ("promotion"), freeing the TMEM
+//    buffer as soon as its last read has landed. Scale words are loaded two
+//    K blocks before use and decoded only then, so no global load is waited
+//    for early. At the end of the tile it converts to bf16 and stores its row.
 // The m-tiles come from the layout's per-expert tile prefix, read on the
 // device: a CTA maps a linear tile id to (expert, m block, n block), and
 // tiles past the device-side total are never visited, so a capacity-sized
 // buffer costs nothing beyond its real rows.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "host_util.h"
+
+#ifndef MOE_GEMM_STAGES_256
+#define MOE_GEMM_STAGES_256 4
+#endif
 
 namespace moe {
 namespace {
@@ -37,20 +46,23 @@ constexpr int BM = 128;
 constexpr int BK = 128;      // one scale block along K = one 128-byte swizzle row
 constexpr int UMMA_K = 32;   // K of one tcgen05.mma for 8-bit operands
 constexpr int kMaxE = 1024;
+constexpr int kTraceWords = 8;
 
 template <int BN>
 struct Cfg {
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kStages = (BN == 256) ? MOE_GEMM_STAGES_256 : 6;
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = BN * BK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kEpiWarps = 4 * (BN / 128);
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kEpiWarps = 4 * (BN / 128);  // one per (TMEM lane quarter, 128 columns)
+  static constexpr int kFirstEpiWarp = 2;           // warp 0: producer, warp 1: MMA
+  static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kNumBars = 2 * kStages + 5;
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem slot, abort flag
-  static constexpr int kTableOffset = kMiscOffset + 16;
+  static constexpr int kTraceOffset = kMiscOffset + 16;          // kTraceWords x u64
+  static constexpr int kTableOffset = kTraceOffset + kTraceWords * 8;
   static constexpr int kSmemBytes = 1024 + kTableOffset + (2 * kMaxE + 1) * 4;
 };
 
@@ -68,6 +80,7 @@ struct Params {
   int64_t M_cap;
   uint16_t* out;
   int32_t* status;
+  unsigned long long* trace;  // optional per-CTA cycle counters
 };
 
 // Bounded wait used while draining: no abort check, only the time limit.
@@ -82,6 +95,18 @@ MOE_DEV uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
+
+// Trace slots (cycles unless noted), summed per CTA.
+enum TraceSlot {
+  kTrKernel = 0,      // whole kernel (thread 0)
+  kTrProdWait = 1,    // producer waiting for a free stage
+  kTrMmaWaitTmem = 2, // MMA waiting for a free TMEM buffer
+  kTrMmaWaitData = 3, // MMA waiting for TMA data
+  kTrUnused4 = 4,
+  kTrUnused5 = 5,
+  kTrUnused6 = 6,
+  kTrKBlocks = 7,     // K blocks this CTA processed (count)
+};
 
 template <int BN>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
@@ -98,11 +123,14 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   uint64_t* mma_done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOffset + 4);
+  unsigned long long* s_trace = reinterpret_cast<unsigned long long*>(smem + C::kTraceOffset);
   int* s_tp = reinterpret_cast<int*>(smem + C::kTableOffset);
   int* s_start = s_tp + (p.E + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const bool tracing = p.trace != nullptr;
+  const long long t_kernel0 = clock64();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -115,6 +143,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
+    for (int i = 0; i < kTraceWords; ++i) s_trace[i] = 0ull;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -151,18 +180,21 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     rows = min(BM, seg_end - row0);
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp < C::kFirstEpiWarp) {
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
       int stage = 0, issued = 0;
       uint32_t phase = 0;
+      unsigned long long t_wait = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
         int e, row0, rows;
         tile_rows(tile, e, row0, rows);
         const int n0 = (tile % num_n) * BN;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
+          const long long t0 = tracing ? clock64() : 0;
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (tracing) t_wait += clock64() - t0;
           uint8_t* sa = smem + stage * C::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
           tma_load_2d(sa, &tmA, kb * BK, row0, &full[stage]);
@@ -172,6 +204,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         }
         if (!ok) break;
       }
+      if (tracing) s_trace[kTrProdWait] = t_wait;
       // Let the last loads land before the CTA can exit.
       const int outstanding = issued < C::kStages ? issued : C::kStages;
       for (int i = 1; i <= outstanding; ++i) {
@@ -180,18 +213,25 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         if (s < 0) { s += C::kStages; ph ^= 1u; }
         drain_wait(&full[s], ph);
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = idesc_f8_f32(BM, BN);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
+      unsigned long long t_tmem = 0, t_data = 0, nkb = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
+          const long long t0 = tracing ? clock64() : 0;
           if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          const long long t1 = tracing ? clock64() : 0;
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          if (tracing) {
+            const long long t2 = clock64();
+            t_tmem += t1 - t0;
+            t_data += t2 - t1;
+            ++nkb;
+          }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
           const uint32_t sb = sa + C::kABytes;
@@ -208,13 +248,18 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         }
         if (!ok) break;
       }
+      if (tracing) {
+        s_trace[kTrMmaWaitTmem] = t_tmem;
+        s_trace[kTrMmaWaitData] = t_data;
+        s_trace[kTrKBlocks] = nkb;
+      }
       // Every MMA issued so far must complete before TMEM is released.
       tc_commit(mma_done);
       drain_wait(mma_done, 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;
+    const int ew = warp - C::kFirstEpiWarp;
     const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
     const int half = ew >> 2;      // which 128-column half of the BN tile
     const int row_in_tile = quarter * 32 + lane;
@@ -222,7 +267,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     const float* wsf = static_cast<const float*>(p.w_scale);
     int acc_buf = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       int e, row0, rows;
       tile_rows(tile, e, row0, rows);
       const int n_tile = tile % num_n;
@@ -231,61 +277,75 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       const bool row_ok = row_in_tile < rows && row < p.M_cap;
       const int64_t wbase = (static_cast<int64_t>(e) * NB + nb) * KB;
 
-      auto scale_at = [&](int kb) -> float {
-        const float sw = p.ue8m0 ? ue8m0_to_f32(ws8[wbase + kb]) : wsf[wbase + kb];
-        float sa = 0.0f;
-        if (row_ok) {
-          if (p.ue8m0) {
-            const uint32_t word = static_cast<const uint32_t*>(
-                p.a_scale)[static_cast<int64_t>(kb >> 2) * p.ld_as + row];
-            sa = ue8m0_to_f32((word >> (8 * (kb & 3))) & 0xFFu);
-          } else {
-            sa = static_cast<const float*>(p.a_scale)[static_cast<int64_t>(row) * p.ld_as + kb];
-          }
+      // Raw scale words, loaded two K blocks before they are used and only
+      // decoded (and multiplied) then, so no load is waited for early.
+      const float* asf = static_cast<const float*>(p.a_scale);
+      const uint32_t* asw = static_cast<const uint32_t*>(p.a_scale);
+      auto load_raw = [&](int kb, uint32_t& ra, uint32_t& rw) {
+        if (kb >= KB) {
+          ra = 0u;
+          rw = 0u;
+          return;
         }
-        return sa * sw;
+        rw = p.ue8m0 ? static_cast<uint32_t>(ws8[wbase + kb]) : __float_as_uint(wsf[wbase + kb]);
+        ra = 0u;
+        if (row_ok)
+          ra = p.ue8m0 ? asw[static_cast<int64_t>(kb >> 2) * p.ld_as + row]
+                       : __float_as_uint(asf[static_cast<int64_t>(row) * p.ld_as + kb]);
+      };
+      auto decode = [&](int kb, uint32_t ra, uint32_t rw) -> float {
+        if (p.ue8m0) return ue8m0_to_f32((ra >> (8 * (kb & 3))) & 0xFFu) * ue8m0_to_f32(rw);
+        return __uint_as_float(ra) * __uint_as_float(rw);
       };
 
-      float acc[128];
+      // Accumulators as packed pairs: one fma.rn.f32x2 promotes two columns.
+      float2 acc[64];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-      float sc_next = scale_at(0);
-      bool ok = true;
-      for (int kb = 0; kb < KB; ++kb) {
-        const float sc = sc_next;
-        if (kb + 1 < KB) sc_next = scale_at(kb + 1);
+      for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
+
+      // One K block: wait for its accumulator, read it from TMEM 16 columns
+      // at a time, fold it in with the block's scale, free the buffer as
+      // soon as the last read has landed.
+      auto kblock = [&](int kb, uint32_t& ra, uint32_t& rw) {
+        if (!ok || kb >= KB) return;
+        const float sc1 = decode(kb, ra, rw);
+        const float2 sc = make_float2(sc1, sc1);
+        load_raw(kb + 2, ra, rw);
         // all lanes leave together: the TMEM loads below are warp-collective
         const bool got = mbar_wait(&tfull[acc_buf], acc_phase, abort_flag, p.status);
-        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          return;
+        }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                static_cast<uint32_t>(acc_buf * BN + half * 128);
-        if constexpr (BN == 256) {
-          // 16-column loads keep the staging registers small next to the
-          // 128 accumulators (10 warps leave 168 registers per thread).
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t v[16];
-            tc_ld16_wait(taddr + c * 16, v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc[c * 16 + j] = fmaf(sc, __uint_as_float(v[j]), acc[c * 16 + j]);
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[16];
+          tc_ld16_wait(taddr + c * 16, v);
+          if (c == 7) {
+            // this TMEM buffer is free once every load from it has completed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc_buf]);
           }
-        } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            tc_ld32_wait(taddr + c * 32, v);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              acc[c * 32 + j] = fmaf(sc, __uint_as_float(v[j]), acc[c * 32 + j]);
-          }
+          for (int j = 0; j < 8; ++j)
+            acc[c * 8 + j] = __ffma2_rn(sc, make_float2(__uint_as_float(v[2 * j]),
+                                                        __uint_as_float(v[2 * j + 1])),
+                                        acc[c * 8 + j]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc_buf]);
         acc_buf ^= 1;
         if (acc_buf == 0) acc_phase ^= 1u;
+      };
+
+      uint32_t ra0, rw0, ra1, rw1;
+      load_raw(0, ra0, rw0);
+      load_raw(1, ra1, rw1);
+      for (int kb0 = 0; kb0 < KB && ok; kb0 += 2) {
+        kblock(kb0 + 0, ra0, rw0);
+        kblock(kb0 + 1, ra1, rw1);
       }
       if (!ok) break;
       if (row_ok) {
@@ -295,10 +355,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
 #pragma unroll
         for (int v = 0; v < 16; ++v) {
           uint4 o;
-          o.x = pack_bf16x2(acc[v * 8 + 0] * wm, acc[v * 8 + 1] * wm);
-          o.y = pack_bf16x2(acc[v * 8 + 2] * wm, acc[v * 8 + 3] * wm);
-          o.z = pack_bf16x2(acc[v * 8 + 4] * wm, acc[v * 8 + 5] * wm);
-          o.w = pack_bf16x2(acc[v * 8 + 6] * wm, acc[v * 8 + 7] * wm);
+          o.x = pack_bf16x2(acc[v * 4 + 0].x * wm, acc[v * 4 + 0].y * wm);
+          o.y = pack_bf16x2(acc[v * 4 + 1].x * wm, acc[v * 4 + 1].y * wm);
+          o.z = pack_bf16x2(acc[v * 4 + 2].x * wm, acc[v * 4 + 2].y * wm);
+          o.w = pack_bf16x2(acc[v * 4 + 3].x * wm, acc[v * 4 + 3].y * wm);
           dst[v] = o;
         }
       }
@@ -310,6 +370,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+  if (tracing && threadIdx.x == 0) {
+    s_trace[kTrKernel] = static_cast<unsigned long long>(clock64() - t_kernel0);
+    for (int i = 0; i < kTraceWords; ++i) p.trace[blockIdx.x * kTraceWords + i] = s_trace[i];
   }
 }
 
@@ -355,6 +419,8 @@ int make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
   return MOE_OK;
 }
 
+std::atomic<unsigned long long*> g_trace{nullptr};
+
 template <int BN>
 int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm, cudaStream_t s) {
   using C = Cfg<BN>;
@@ -373,6 +439,11 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm, cuda
 
 }  // namespace
 }  // namespace moe
+
+extern "C" int moe_gemm_set_trace(uint64_t* d_trace) {
+  moe::g_trace.store(reinterpret_cast<unsigned long long*>(d_trace));
+  return MOE_OK;
+}
 
 extern "C" int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale_layout,
                                 int64_t ld_as, const int32_t* start, const int32_t* tile_prefix,
@@ -421,6 +492,7 @@ extern "C" int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale
   prm.M_cap = M_cap;
   prm.out = out;
   prm.status = d_status;
+  prm.trace = moe::g_trace.load();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return BN == 256 ? moe::launch<256>(ta, tb, prm, s) : moe::launch<128>(ta, tb, prm, s);
 }

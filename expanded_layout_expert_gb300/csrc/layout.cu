@@ -26,6 +26,9 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kPairsPerWarp = 256;
 constexpr int kChunk = kWarps * kPairsPerWarp;  // pairs per block
 constexpr int kMaxE = 1024;
+constexpr int kPerThread = kChunk / kThreads;   // pairs per thread in the count pass
+constexpr int kRounds = kPairsPerWarp / 32;     // 32-pair rounds per warp in the rank pass
+constexpr int kScanSmem = 6144;                 // (expert, block) counts staged in shared memory
 
 inline int64_t num_chunks(int64_t T, int K) {
   const int64_t pairs = T * K;
@@ -69,6 +72,7 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(
     int32_t* __restrict__ status) {
   __shared__ int hist[kMaxE];
   __shared__ int s_start[kMaxE];
+  __shared__ int s_cnt[kScanSmem];
   __shared__ int warp_tot[kWarps];
   __shared__ int s_last;
   const int tid = threadIdx.x;
@@ -77,16 +81,18 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(
 
   const int64_t npairs = valid_rows(d_n_valid, T) * K;
   const int64_t p0 = static_cast<int64_t>(blockIdx.x) * kChunk;
-  for (int i = tid; i < kChunk; i += kThreads) {
-    const int64_t p = p0 + i;
-    if (p >= npairs) break;
-    const int id = ids[p];
-    if (id < 0) continue;
-    if (id >= E) {
-      set_status(status, MOE_ERR_DEVICE_CHECK);
-      continue;
-    }
-    atomicAdd(&hist[id], 1);
+  // all of this thread's ids first (independent loads), then the counting
+  int idv[kPerThread];
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int64_t p = p0 + j * kThreads + tid;
+    idv[j] = (p < npairs) ? ids[p] : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int id = idv[j];
+    if (id >= E) set_status(status, MOE_ERR_DEVICE_CHECK);
+    else if (id >= 0) atomicAdd(&hist[id], 1);
   }
   __syncthreads();
   for (int e = tid; e < E; e += kThreads) counts[static_cast<int64_t>(e) * nb + blockIdx.x] = hist[e];
@@ -97,20 +103,32 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(
   if (!s_last) return;
   __threadfence();
 
-  // Last block. Per expert: exclusive scan over the blocks' counts.
+  // Last block. The per-(expert, block) counts go through shared memory when
+  // they fit (one round of parallel loads instead of a chain of dependent
+  // ones); per expert, an exclusive scan over the blocks.
   const int lane = tid & 31, warp = tid >> 5;
+  const int64_t n_offs = static_cast<int64_t>(E) * nb;
+  const bool staged = n_offs <= kScanSmem;
+  if (staged) {
+    for (int64_t i = tid; i < n_offs; i += kThreads) s_cnt[i] = __ldcg(&counts[i]);
+    __syncthreads();
+  }
   for (int e = warp; e < E; e += kWarps) {
     int carry = 0;
     for (int b0 = 0; b0 < nb; b0 += 32) {
       const int b = b0 + lane;
-      const int c = (b < nb) ? __ldcg(&counts[static_cast<int64_t>(e) * nb + b]) : 0;
+      const int64_t i = static_cast<int64_t>(e) * nb + b;
+      const int c = (b < nb) ? (staged ? s_cnt[i] : __ldcg(&counts[i])) : 0;
       int incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      if (b < nb) offs[static_cast<int64_t>(e) * nb + b] = carry + incl - c;
+      if (b < nb) {
+        if (staged) s_cnt[i] = carry + incl - c;
+        else offs[i] = carry + incl - c;
+      }
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) hist[e] = carry;  // count of expert e
@@ -152,8 +170,11 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(
     if (rows_total > M_cap) set_status(status, MOE_ERR_DEVICE_CHECK);
   }
   __syncthreads();
-  const int64_t n_offs = static_cast<int64_t>(E) * nb;
-  for (int64_t i = tid; i < n_offs; i += kThreads) offs[i] += s_start[i / nb];
+  if (staged) {
+    for (int64_t i = tid; i < n_offs; i += kThreads) offs[i] = s_cnt[i] + s_start[i / nb];
+  } else {
+    for (int64_t i = tid; i < n_offs; i += kThreads) offs[i] += s_start[i / nb];
+  }
   if (tid == 0) *ticket = 0u;  // ready for the next call
 }
 
@@ -174,14 +195,17 @@ __global__ void __launch_bounds__(kThreads) layout_rank_kernel(
   const int64_t base_p = static_cast<int64_t>(blockIdx.x) * kChunk + warp * kPairsPerWarp;
   int* my = wcnt + warp * E;
 
-  // Pass 1: this warp's pairs per expert.
-  for (int r = 0; r < kPairsPerWarp; r += 32) {
-    const int64_t p = base_p + r + lane;
-    if (p < npairs) {
-      const int id = ids[p];
-      if (id >= 0 && id < E) atomicAdd(&my[id], 1);
-    }
+  // This warp's pairs, loaded up front (independent loads).
+  int idv[kRounds];
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j) {
+    const int64_t p = base_p + j * 32 + lane;
+    idv[j] = (p < npairs) ? ids[p] : -1;
   }
+  // Pass 1: this warp's pairs per expert.
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j)
+    if (idv[j] >= 0 && idv[j] < E) atomicAdd(&my[idv[j]], 1);
   __syncthreads();
   // Pass 2: per expert, exclusive over the warps, on top of the block's base.
   for (int e = tid; e < E; e += kThreads) {
@@ -196,14 +220,11 @@ __global__ void __launch_bounds__(kThreads) layout_rank_kernel(
   // Pass 3: in (token, k) order, 32 pairs at a time; lanes holding the same
   // expert are ranked by lane, the lowest of them advances the counter.
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int r = 0; r < kPairsPerWarp; r += 32) {
-    const int64_t p = base_p + r + lane;
-    int id = -1;
-    bool valid = false;
-    if (p < npairs) {
-      id = ids[p];
-      valid = (id >= 0 && id < E);
-    }
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j) {
+    const int64_t p = base_p + j * 32 + lane;
+    const int id = idv[j];
+    const bool valid = (id >= 0 && id < E);
     const int key = valid ? id : (E + static_cast<int>(lane));
     const unsigned peers = __match_any_sync(0xffffffffu, key);
     int dst = -1;

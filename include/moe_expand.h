@@ -222,6 +222,14 @@ int moe_combine(const uint16_t* down_out, const int32_t* src2dst, const float* r
                 const int32_t* d_n_valid, int64_t T, int H, int K, uint16_t* y,
                 moe_stream_t stream);
 
+/* Host. Diagnostics: when d_trace is not NULL, every later moe_grouped_gemm
+ * launch writes 8 uint64 counters per CTA (grid = SM count) to d_trace:
+ * kernel cycles, producer cycles waiting for a free stage, MMA cycles waiting
+ * for a free accumulator, MMA cycles waiting for operand data, three unused
+ * words, and K blocks processed. NULL turns it off. Not thread-safe with
+ * respect to concurrent launches on other threads. */
+int moe_gemm_set_trace(uint64_t* d_trace);
+
 /* Host. Text of the last error raised on this thread (never NULL). */
 const char* moe_last_error_string(void);
 

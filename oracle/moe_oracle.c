@@ -345,9 +345,9 @@ int orc_gemm_rows(const uint8_t* A, int64_t lda, const void* A_scale, int scale_
 /* silu(g)*u, then per-token-group fp8 quantisation of down_proj's input    */
 /* (_run_contiguous_gemm's default branch: silu_and_mul into a bf16 tensor, */
 /* then per-token-group quant with group 128). Gate is the first I columns, */
-/* up the last I. Per group: amax = max(max|h|, 1e-10), s = amax/448, codes */
-/* h/s rounded to e4m3 (the quantiser formula of                             */
-/* _situ_mul_quant_contig_kernel). With fp32 scales the row's top-k weight  */
+/* up the last I. Per group: amax = max(max|h|, 1e-10), stored scale         */
+/* s = amax/448, codes h * (448/amax) rounded to e4m3 (the quantiser formula */
+/* of _situ_mul_quant_contig_kernel). With fp32 scales the row's top-k weight */
 /* is folded into the stored scale, s*w (SGLang PR 37261, Modifications /    */
 /* Core: dequant is q*scale and down_proj is linear, so the per-row factor  */
 /* moves into the scale). With ue8m0 scales s is rounded up to a power of   */
@@ -386,8 +386,9 @@ int orc_act_quant_rows(const uint16_t* gu, int64_t n, int I, const float* row_w,
             if (scale_layout == ORC_SCALE_F32) {
                 float w = row_w ? row_w[i] : 1.0f;
                 float stored = s * w;
+                float inv = 448.0f / amax;      /* codes are h * (448 / amax) */
                 for (int j = gi * 128; j < gi * 128 + 128; ++j) {
-                    float v = h[j] / s;
+                    float v = h[j] * inv;
                     di[i * I + j] = orc_e4m3_encode(v);
                 }
                 ((float*)di_scale)[i * ld_ds + gi] = stored;

@@ -23,7 +23,7 @@
  *
  * Parity unpinned (readings, covered by tolerance rather than by a pin):
  *   - order of pairs inside one expert's segment (ascending token, then k);
- *   - h/s versus h*(448/amax) in the activation quantiser;
+ *   - codes as h*(448/amax) (the pages' formula) rather than h/s;
  *   - the bf16 rounding of silu(g)*u before quantisation;
  *   - the ue8m0 output weighting in fp32 with one bf16 rounding.
  */

@@ -106,6 +106,8 @@ PARITY_CONFIGS = (
                 seed=13, routing="uniform", scale_mode=SCALE_UE8M0),
     LayerConfig("mid_padded", T=512, H=1024, I=512, E=8, K=4, align=128,
                 seed=14, routing="uniform", n_valid=150, garbage_tail=True),
+    LayerConfig("small_h384", T=96, H=384, I=128, E=6, K=2, align=8, seed=15,
+                routing="uniform", inactive_frac=0.10),
 )
 
 
