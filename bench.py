@@ -51,6 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-sample-seconds", type=float, default=15.0)
     ap.add_argument("--gemm-tile-n128", action="store_true",
                     help="force 128-column GEMM tiles (tuning comparison)")
+    ap.add_argument("--gemm-cta-pair", action="store_true",
+                    help="256 x 256 GEMM tiles on CTA pairs (tuning comparison)")
     return ap.parse_args(argv)
 
 
@@ -199,7 +201,8 @@ def run_ours(args, world, rank, local):
     x_q, x_s, ids, w = d["x_q"], d["x_s"], d["topk_ids"], d["topk_w"]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     names = ["layout", "scatter", "gemm1", "act_quant", "gemm2", "combine"]
-    gflags = mx.MOE_GEMM_TILE_N128 if args.gemm_tile_n128 else 0
+    gflags = (mx.MOE_GEMM_TILE_N128 if args.gemm_tile_n128 else 0) | \
+        (mx.MOE_GEMM_CTA_PAIR if args.gemm_cta_pair else 0)
 
     def step(ev=None):
         def mark(i):

@@ -67,6 +67,7 @@ typedef struct CUstream_st* moe_stream_t; /* the same type as cudaStream_t */
 #define MOE_FOLD_WEIGHT_INTO_SCALE 1 /* fp32 path: store s*w as down_proj's input scale */
 #define MOE_WEIGHT_OUTPUT_ROWS     2 /* ue8m0 path: multiply the down_proj output row by w */
 #define MOE_GEMM_TILE_N128        16 /* tuning: use 128-column GEMM tiles even when N % 256 == 0 */
+#define MOE_GEMM_CTA_PAIR         32 /* tuning: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2) */
 
 /* Rows per grouped-GEMM tile; tile_prefix counts tiles of this height. */
 #define MOE_BLOCK_M 128

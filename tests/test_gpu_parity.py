@@ -92,7 +92,7 @@ def test_scatter_bit_exact(mx, cases, name):
         assert np.array_equal(xs[:, :tot], ref["xe_s"][:, :tot])
 
 
-@pytest.mark.parametrize("tile_flag", [0, 16], ids=["bn_auto", "bn128"])
+@pytest.mark.parametrize("tile_flag", [0, 16, 32], ids=["default", "bn128", "cta_pair"])
 @pytest.mark.parametrize("name", NAMES)
 def test_gate_up_gemm(mx, cases, name, tile_flag):
     c = cases[name]
