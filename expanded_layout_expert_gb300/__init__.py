@@ -14,7 +14,8 @@ from typing import Optional
 import torch
 
 from . import _capi
-from ._capi import (MOE_BLOCK_M, MOE_FOLD_WEIGHT_INTO_SCALE, MOE_GEMM_CTA_PAIR, MOE_GEMM_TILE_N128,
+from ._capi import (MOE_BLOCK_M, MOE_FOLD_WEIGHT_INTO_SCALE, MOE_GEMM_CTA_PAIR, MOE_GEMM_PER_KBLOCK_PROMOTION,
+                    MOE_GEMM_TILE_N128,
                     MOE_SCALE_F32_ROWMAJOR, MOE_SCALE_UE8M0_PACKED_COLMAJOR,
                     MOE_WEIGHT_OUTPUT_ROWS, MoEError, check, load)
 
@@ -22,7 +23,8 @@ __all__ = [
     "expanded_capacity", "workspace_size", "expand_layout", "expand_scatter", "grouped_gemm",
     "act_quant", "grouped_ffn", "combine", "ExpandedMoELayer", "Layout", "MoEError",
     "MOE_SCALE_F32_ROWMAJOR", "MOE_SCALE_UE8M0_PACKED_COLMAJOR", "MOE_FOLD_WEIGHT_INTO_SCALE",
-    "MOE_WEIGHT_OUTPUT_ROWS", "MOE_GEMM_TILE_N128", "MOE_GEMM_CTA_PAIR", "MOE_BLOCK_M",
+    "MOE_WEIGHT_OUTPUT_ROWS", "MOE_GEMM_TILE_N128", "MOE_GEMM_CTA_PAIR",
+    "MOE_GEMM_PER_KBLOCK_PROMOTION", "MOE_BLOCK_M",
     "scale_layout_of",
 ]
 

@@ -254,6 +254,73 @@ constexpr uint32_t idesc_f8_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
 }
 
+// ---- block-scaled MMA (kind::mxf8f6f4): the tensor core applies one ue8m0
+// scale per row of A and per row of B to each K = 32 step.
+
+// Generic-proxy writes to shared memory become visible to the async proxy
+// (tcgen05.cp, TMA) once this fence has been executed by the writer.
+MOE_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Shared-memory descriptor for a source of 16-byte rows stored back to back
+// without swizzling: 8-row core matrices 128 bytes apart (stride byte
+// offset); one core matrix wide, so the leading byte offset is unused.
+MOE_DEV uint64_t rows16_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address >> 4
+  d |= static_cast<uint64_t>(128 >> 4) << 32;           // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version (tcgen05)
+  return d;                                             // swizzle mode 0: none
+}
+
+// Copies 32 rows x 16 bytes from shared memory into TMEM lanes 0-31,
+// 4 columns from `taddr`, repeated in all four 32-lane quarters.
+MOE_DEV void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// D[tmem] (+)= (sfA * A)[smem] * (sfB * B)[smem]^T, e4m3 operands, K = 32,
+// one ue8m0 scale per row of A (read from TMEM at sfa) and per row of B
+// (at sfb); the byte of each 32-bit scale word is chosen in idesc.
+MOE_DEV void tc_mma_mx8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of the block-scaled MMA: D = f32 (implied),
+// A = B = e4m3, both K-major, scale factors ue8m0. The scale byte selectors
+// (bits 4-5 for B, 29-30 for A) are added per instruction.
+constexpr uint32_t idesc_mx8(int M, int N) {
+  return (0u << 7)                                // A format: e4m3
+         | (0u << 10)                             // B format: e4m3
+         | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
+         | (1u << 23)                             // scale factor type: ue8m0
+         | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
+}
+MOE_DEV uint32_t idesc_with_sf(uint32_t idesc, uint32_t a_byte, uint32_t b_byte) {
+  return idesc | (b_byte << 4) | (a_byte << 29);
+}
+
+// Marks 32 registers as written after a tcgen05.wait::ld that was issued
+// earlier, so none of their uses can move above that wait.
+MOE_DEV void tc_regs_landed(uint32_t (&v)[32]) {
+  asm volatile(""
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]),
+                 "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                 "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]),
+                 "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+               :
+               : "memory");
+}
+
 // ue8m0 exponent byte -> 2^(byte-127) as fp32 (byte 0 is the subnormal 2^-127).
 MOE_DEV float ue8m0_to_f32(uint32_t b) {
   return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);

@@ -35,8 +35,12 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "gemm_host.h"
 #include "host_util.h"
 
+#ifndef MOE_GEMM_STAGED_MAX_KB
+#define MOE_GEMM_STAGED_MAX_KB 24
+#endif
 #ifndef MOE_GEMM_STAGES_256
 #define MOE_GEMM_STAGES_256 4
 #endif
@@ -50,7 +54,7 @@ constexpr int UMMA_K = 32;   // K of one tcgen05.mma for 8-bit operands
 constexpr int kMaxE = 1024;
 constexpr int kTraceWords = 8;
 
-template <int BN>
+template <int BN, bool Staged>
 struct Cfg {
   static constexpr int kStages = (BN == 256) ? MOE_GEMM_STAGES_256 : 6;
   static constexpr int kABytes = BM * BK;
@@ -76,8 +80,16 @@ struct Cfg {
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem slot, abort flag
   static constexpr int kTraceOffset = kMiscOffset + 16;          // kTraceWords x u64
-  static constexpr int kTableOffset = kTraceOffset + kTraceWords * 8;
-  static constexpr int kSmemBytes = 1024 + kTableOffset + (2 * kMaxE + 1) * 4;
+  // Staged: per epilogue warp, 32 rows x 64 bf16 columns go through shared
+  // memory for coalesced stores. It pays when tiles are short in K (the
+  // store is a larger share of a tile) and costs L1 capacity otherwise (the
+  // carve-out leaves less room for the cached activation-scale rows).
+  static constexpr int kStoreOffset = (kTraceOffset + kTraceWords * 8 + 1023) / 1024 * 1024;
+  static constexpr int kStoreBytesPerWarp = Staged ? 32 * 128 : 0;
+  // per-expert tables in shared memory when E <= kSmemE (else read from global)
+  static constexpr int kTableOffset = kStoreOffset + kEpiWarps * kStoreBytesPerWarp;
+  static constexpr int kSmemE = Staged ? 96 : 512;
+  static constexpr int kSmemBytes = 1024 + kTableOffset + (2 * kSmemE + 1) * 4;
 };
 
 struct Params {
@@ -122,11 +134,11 @@ enum TraceSlot {
   kTrKBlocks = 7,     // K blocks this CTA processed (count)
 };
 
-template <int BN>
-__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
+template <int BN, bool Staged>
+__global__ void __launch_bounds__(Cfg<BN, Staged>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, Staged>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -138,8 +150,12 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOffset + 4);
   unsigned long long* s_trace = reinterpret_cast<unsigned long long*>(smem + C::kTraceOffset);
-  int* s_tp = reinterpret_cast<int*>(smem + C::kTableOffset);
-  int* s_start = s_tp + (p.E + 1);
+  // per-expert tables: shared memory for up to kSmemE experts, else global
+  const bool smem_tables = p.E <= C::kSmemE;
+  int* t_tp = reinterpret_cast<int*>(smem + C::kTableOffset);
+  int* t_start = t_tp + (p.E + 1);
+  const int* s_tp = smem_tables ? t_tp : p.tile_prefix;
+  const int* s_start = smem_tables ? t_start : p.start;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -166,8 +182,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
-  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_tp[i] = p.tile_prefix[i];
-  for (int i = threadIdx.x; i < p.E; i += blockDim.x) s_start[i] = p.start[i];
+  if (smem_tables) {
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) t_tp[i] = p.tile_prefix[i];
+    for (int i = threadIdx.x; i < p.E; i += blockDim.x) t_start[i] = p.start[i];
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -379,17 +397,62 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         kblock(kb0 + 1, ra1, rw1);
       }
       if (!ok) break;
-      if (row_ok) {
-        const float wm = p.weight_rows ? p.row_w[row] : 1.0f;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.N + col0);
+      if constexpr (Staged) {
+      // Store through shared memory: each thread writes its row's 64-column
+      // slices (swizzled, conflict-free), then the warp writes 4 rows of 128
+      // contiguous bytes per instruction.
+      {
+        const float wm = (p.weight_rows && row_ok) ? p.row_w[row] : 1.0f;
+        uint8_t* stg = smem + C::kStoreOffset + ew * C::kStoreBytesPerWarp;
+        const uint32_t stg_s = smem_u32(stg);
+        const int row_w0 = row0 + quarter * 32;          // this warp's first row
+        const int rows_w = rows - quarter * 32;          // valid rows of this warp
 #pragma unroll
-        for (int v = 0; v < C::kColsPerWarp / 8; ++v) {
-          uint4 o;
-          o.x = pack_bf16x2(acc[v * 4 + 0].x * wm, acc[v * 4 + 0].y * wm);
-          o.y = pack_bf16x2(acc[v * 4 + 1].x * wm, acc[v * 4 + 1].y * wm);
-          o.z = pack_bf16x2(acc[v * 4 + 2].x * wm, acc[v * 4 + 2].y * wm);
-          o.w = pack_bf16x2(acc[v * 4 + 3].x * wm, acc[v * 4 + 3].y * wm);
-          dst[v] = o;
+        for (int ps = 0; ps < C::kColsPerWarp / 64; ++ps) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float2* a2 = &acc[ps * 32 + c * 4];
+            const uint32_t x0 = pack_bf16x2(a2[0].x * wm, a2[0].y * wm);
+            const uint32_t x1 = pack_bf16x2(a2[1].x * wm, a2[1].y * wm);
+            const uint32_t x2 = pack_bf16x2(a2[2].x * wm, a2[2].y * wm);
+            const uint32_t x3 = pack_bf16x2(a2[3].x * wm, a2[3].y * wm);
+            const uint32_t off = static_cast<uint32_t>(lane * 128 + ((c ^ (lane & 7)) << 4));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg_s + off), "r"(x0),
+                         "r"(x1), "r"(x2), "r"(x3)
+                         : "memory");
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3);
+            const int c = lane & 7;
+            uint4 v;
+            const uint32_t off = static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(stg_s + off)
+                         : "memory");
+            const int grow = row_w0 + r;
+            if (r < rows_w && grow < p.M_cap)
+              *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(grow) * p.N + col0 + ps * 64 +
+                                        c * 8) = v;
+          }
+          __syncwarp();
+        }
+      }
+      } else {
+        if (row_ok) {
+          const float wm = p.weight_rows ? p.row_w[row] : 1.0f;
+          uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.N + col0);
+#pragma unroll
+          for (int v = 0; v < C::kColsPerWarp / 8; ++v) {
+            uint4 o;
+            o.x = pack_bf16x2(acc[v * 4 + 0].x * wm, acc[v * 4 + 0].y * wm);
+            o.y = pack_bf16x2(acc[v * 4 + 1].x * wm, acc[v * 4 + 1].y * wm);
+            o.z = pack_bf16x2(acc[v * 4 + 2].x * wm, acc[v * 4 + 2].y * wm);
+            o.w = pack_bf16x2(acc[v * 4 + 3].x * wm, acc[v * 4 + 3].y * wm);
+            dst[v] = o;
+          }
         }
       }
     }
@@ -741,63 +804,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
-
-// 2-D uint8 tensor [outer, inner] with row stride `stride` bytes; box of
-// box_outer rows x 128 bytes, 128-byte swizzle, out-of-range rows read as 0.
-int make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t stride,
-              uint32_t box_outer) {
-  EncodeTiledFn enc = encode_fn();
-  if (enc == nullptr) {
-    set_error("cuTensorMapEncodeTiled is not available from the driver");
-    return MOE_ERR_CUDA;
-  }
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {stride};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    set_error("cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
-    return MOE_ERR_CUDA;
-  }
-  return MOE_OK;
-}
-
 std::atomic<unsigned long long*> g_trace{nullptr};
 
-template <int BN>
+template <int BN, bool Staged>
 int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm, cudaStream_t s) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, Staged>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<BN, Staged>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
       return check_launch("cudaFuncSetAttribute(grouped_gemm_kernel)");
     attr_set[dev] = true;
   }
-  grouped_gemm_kernel<BN><<<device_sm_count(), C::kThreads, C::kSmemBytes, s>>>(ta, tb, prm);
+  grouped_gemm_kernel<BN, Staged><<<device_sm_count(), C::kThreads, C::kSmemBytes, s>>>(ta, tb, prm);
   return check_launch("grouped_gemm_kernel");
 }
 
@@ -849,12 +870,35 @@ extern "C" int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale
               "moe_grouped_gemm: A, W and out must be 16-byte aligned");
   MOE_REQUIRE_DEVICE();
 
+  // Power-of-two scales go to the tensor core's block scaling.
+  const bool block_scaled = scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR && N % 256 == 0 &&
+                            !(flags & (MOE_GEMM_TILE_N128 | MOE_GEMM_CTA_PAIR |
+                                       MOE_GEMM_PER_KBLOCK_PROMOTION));
+  if (block_scaled) {
+    moe::MxGemmArgs a;
+    a.A = A;
+    a.A_scale = static_cast<const uint32_t*>(A_scale);
+    a.ld_as = ld_as;
+    a.start = start;
+    a.tile_prefix = tile_prefix;
+    a.d_total = d_total;
+    a.W = W;
+    a.W_scale = static_cast<const uint8_t*>(W_scale);
+    a.row_w = (flags & MOE_WEIGHT_OUTPUT_ROWS) ? row_w : nullptr;
+    a.E = E;
+    a.N = N;
+    a.Kd = Kd;
+    a.M_cap = M_cap;
+    a.out = out;
+    a.status = d_status;
+    return moe::launch_grouped_gemm_mx(a, reinterpret_cast<cudaStream_t>(stream));
+  }
   const bool pair = N % 256 == 0 && (flags & MOE_GEMM_CTA_PAIR) && !(flags & MOE_GEMM_TILE_N128);
   const int BN = (N % 256 == 0 && !(flags & MOE_GEMM_TILE_N128)) ? 256 : 128;
   CUtensorMap ta, tb;
-  int rc = moe::make_tmap(&ta, A, Kd, M_cap, Kd, moe::BM);
+  int rc = moe::make_tmap_k128(&ta, A, Kd, M_cap, Kd, moe::BM);
   if (rc != MOE_OK) return rc;
-  rc = moe::make_tmap(&tb, W, Kd, static_cast<uint64_t>(E) * N, Kd, pair ? 128 : BN);
+  rc = moe::make_tmap_k128(&tb, W, Kd, static_cast<uint64_t>(E) * N, Kd, pair ? 128 : BN);
   if (rc != MOE_OK) return rc;
   moe::Params prm;
   prm.a_scale = A_scale;
@@ -875,5 +919,10 @@ extern "C" int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale
   prm.trace = moe::g_trace.load();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (pair) return moe::launch_pair(ta, tb, prm, s);
-  return BN == 256 ? moe::launch<256>(ta, tb, prm, s) : moe::launch<128>(ta, tb, prm, s);
+  // Short-K GEMMs (down_proj) spend a larger share of each tile on the
+  // store, so they take the staged store; long-K ones keep the L1 room.
+  const bool staged = (Kd / 128) <= MOE_GEMM_STAGED_MAX_KB;
+  if (BN == 256)
+    return staged ? moe::launch<256, true>(ta, tb, prm, s) : moe::launch<256, false>(ta, tb, prm, s);
+  return staged ? moe::launch<128, true>(ta, tb, prm, s) : moe::launch<128, false>(ta, tb, prm, s);
 }

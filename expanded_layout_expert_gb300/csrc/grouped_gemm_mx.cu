@@ -1,0 +1,395 @@
+// Block-scaled grouped GEMM for power-of-two (ue8m0) scales: the scales are
+// applied inside the tensor core (tcgen05.mma kind::mxf8f6f4.block_scale), so
+// a tile accumulates its whole K range in one TMEM accumulator and the
+// epilogue runs once per tile instead of once per K block.
+//
+//   out[r, n] = bf16( w_r * sum_kb 2^(a[r,kb]-127) * 2^(b[e,n/128,kb]-127)
+//                               * sum_{k in block kb} A[r, k] * W[e, n, k] )
+//
+// with w_r = row_w[r] on the weighted-output path and 1 otherwise (the ue8m0
+// path of the expanded MoE layer: SGLang moe_runner/deep_gemm.py,
+// DeepGemmMoeQuantInfo with ue8m0 scales; the per-row output weighting of
+// SGLang PR 20096, "apply topk weights to down_output").
+//
+// Each 128-wide K block carries one activation scale per row and one weight
+// scale per 128 output columns. The tensor core takes one ue8m0 scale per row
+// of A and of B for every K = 32 step, so the four steps of a K block simply
+// reuse the block's scale; a 32-bit scale word packs four K blocks and the
+// instruction descriptor selects the byte.
+//
+// Roles (one persistent CTA per SM, 384 threads):
+//  - warp 0, one lane: TMA producer of the A (128 x 128 B) and W (256 x
+//    128 B) tiles, 128-byte swizzle, into a ring of shared-memory stages.
+//  - warp 2: scale loader. Per group of four K blocks it reads the tile's
+//    128 packed activation-scale words (coalesced) and the two weight-scale
+//    words, and writes them to a shared-memory slot in the order the
+//    32-lane TMEM copy expects: the 16 bytes of lane i hold the words of
+//    rows i, i+32, i+64, i+96 (so TMEM column j of lane i is row i + 32 j).
+//  - warp 1, one lane: MMA issuer. At the start of each group it copies the
+//    slot into TMEM (tcgen05.cp 32x128b.warpx4, ordered before the MMAs that
+//    read it), then issues four K = 32 block-scaled MMAs per K block into
+//    the tile's accumulator.
+//  - warps 4..11: epilogue. Two warps per TMEM lane quarter, 128 columns
+//    each: read the finished accumulator (4 x 32 columns, one wait), free it
+//    for the next tile, scale by the row weight, convert to bf16 and store.
+// TMEM: columns 0-255 the accumulator, 256 + 16 s the scale slot s
+// (A: 4 columns, B: 8 columns).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "gemm_host.h"
+#include "host_util.h"
+
+namespace moe {
+namespace {
+
+namespace mx {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;
+constexpr int UMMA_K = 32;
+constexpr int kMaxE = 1024;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK;
+constexpr int kBBytes = BN * BK;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kSfSlots = 4;              // groups of four K blocks in flight
+constexpr int kSfBytesA = 32 * 16;       // 128 rows, one word each
+constexpr int kSfBytesB = 2 * 32 * 16;   // 256 columns, one word each
+constexpr int kSfSlotBytes = kSfBytesA + kSfBytesB;
+constexpr int kEpiWarps = 8;
+constexpr int kFirstEpiWarp = 4;
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+constexpr int kTmemCols = 512;
+constexpr int kSfCol = 256;
+constexpr int kSfSlotCols = 16;
+
+constexpr int kSfOffset = kStages * kStageBytes;
+constexpr int kBarOffset = kSfOffset + kSfSlots * kSfSlotBytes;
+constexpr int kNumBars = 2 * kStages + 2 * kSfSlots + 3;
+constexpr int kMiscOffset = kBarOffset + kNumBars * 8;   // tmem slot, abort flag
+constexpr int kTableOffset = kMiscOffset + 16;           // tile prefix (E+1), start (E)
+constexpr int kSmemBytes = 1024 + kTableOffset + (2 * kMaxE + 1) * 4;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kSfCol + kSfSlots * kSfSlotCols <= kTmemCols, "TMEM budget");
+
+struct Params {
+  const uint32_t* a_scale;
+  int64_t ld_as;
+  const uint8_t* w_scale;
+  const int32_t* start;
+  const int32_t* tile_prefix;
+  const int32_t* d_total;
+  const float* row_w;
+  int E, N, Kd;
+  int64_t M_cap;
+  uint16_t* out;
+  int32_t* status;
+};
+
+MOE_DEV void drain(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return;
+  }
+}
+
+MOE_DEV uint32_t bf16x2_bits(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+  uint64_t* empty = full + kStages;
+  uint64_t* sf_full = empty + kStages;
+  uint64_t* sf_empty = sf_full + kSfSlots;
+  uint64_t* tfull = sf_empty + kSfSlots;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* mma_done = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOffset);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOffset + 4);
+  int* s_tp = reinterpret_cast<int*>(smem + kTableOffset);
+  int* s_start = s_tp + (p.E + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kSfSlots; ++s) {
+      mbar_init(&sf_full[s], 1);
+      mbar_init(&sf_empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, kEpiWarps);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_tp[i] = p.tile_prefix[i];
+  for (int i = threadIdx.x; i < p.E; i += blockDim.x) s_start[i] = p.start[i];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int total = *p.d_total;
+  if (total > p.M_cap) total = static_cast<int>(p.M_cap);
+  const int num_n = p.N / BN;
+  const int num_tiles = s_tp[p.E] * num_n;
+  const int KB = p.Kd / BK;
+  const int NB = p.N / 128;
+
+  auto tile_rows = [&](int tile, int& e, int& row0, int& rows) {
+    const int m = tile / num_n;
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_tp[mid] <= m) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    row0 = s_start[e] + (m - s_tp[e]) * BM;
+    const int seg_end = (e + 1 < p.E) ? min(s_start[e + 1], total) : total;
+    rows = min(BM, seg_end - row0);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        int e, row0, rows;
+        tile_rows(tile, e, row0, rows);
+        const int n0 = (tile % num_n) * BN;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          uint8_t* sa = smem + stage * kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          tma_load_2d(sa, &tmA, kb * BK, row0, &full[stage]);
+          tma_load_2d(sa + kABytes, &tmB, kb * BK, e * p.N + n0, &full[stage]);
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      // let the last loads land before the CTA can exit
+      const int outstanding = issued < kStages ? issued : kStages;
+      for (int i = 1; i <= outstanding; ++i) {
+        int s = stage - i;
+        uint32_t ph = phase;
+        if (s < 0) { s += kStages; ph ^= 1u; }
+        drain(&full[s], ph);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_mx8(BM, BN);
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, sphase = 0, acc_phase = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(kSfCol + slot * kSfSlotCols);
+          if ((kb & 3) == 0) {
+            if (!mbar_wait(&sf_full[slot], sphase, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t ss = smem_u32(smem + kSfOffset + slot * kSfSlotBytes);
+            tc_cp_32x128b_x4(sf_tmem + 0, rows16_desc(ss));
+            tc_cp_32x128b_x4(sf_tmem + 4, rows16_desc(ss + kSfBytesA));
+            tc_cp_32x128b_x4(sf_tmem + 8, rows16_desc(ss + kSfBytesA + 512));
+          }
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          const uint32_t id = idesc_with_sf(idesc, kb & 3, kb & 3);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k)
+            tc_mma_mx8(tmem_base, sw128_kmajor_desc(sa + k * UMMA_K),
+                       sw128_kmajor_desc(sb + k * UMMA_K), id, sf_tmem, sf_tmem + 4,
+                       (kb > 0 || k > 0) ? 1u : 0u);
+          tc_commit(&empty[stage]);
+          if ((kb & 3) == 3 || kb == KB - 1) {
+            tc_commit(&sf_empty[slot]);
+            if (++slot == kSfSlots) { slot = 0; sphase ^= 1u; }
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tfull);
+        acc_phase ^= 1u;
+      }
+      // every MMA issued so far must complete before TMEM is released
+      tc_commit(mma_done);
+      drain(mma_done, 0);
+    }
+  } else if (warp == 2) {
+    // -------------------------------------------------------- scale loader
+    int slot = 0;
+    uint32_t sphase = 0;
+    const int KG = (KB + 3) / 4;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int e, row0, rows;
+      tile_rows(tile, e, row0, rows);
+      const int nb0 = (tile % num_n) * (BN / 128);
+      bool ok = true;
+      for (int g = 0; g < KG; ++g) {
+        const bool got = mbar_wait(&sf_empty[slot], sphase ^ 1u, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        uint32_t a[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t r = static_cast<int64_t>(row0) + lane + 32 * j;
+          a[j] = r < p.M_cap ? p.a_scale[static_cast<int64_t>(g) * p.ld_as + r] : 0x7F7F7F7Fu;
+        }
+        uint32_t w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint8_t* ws = p.w_scale + (static_cast<int64_t>(e) * NB + nb0 + h) * KB + 4 * g;
+          uint32_t word = 0;
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            word |= static_cast<uint32_t>(4 * g + b < KB ? ws[b] : 127u) << (8 * b);
+          w[h] = word;
+        }
+        const uint32_t ss = smem_u32(smem + kSfOffset + slot * kSfSlotBytes);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ss + lane * 16), "r"(a[0]),
+                     "r"(a[1]), "r"(a[2]), "r"(a[3])
+                     : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(ss + kSfBytesA + lane * 16),
+                     "r"(w[0])
+                     : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(ss + kSfBytesA + 512 +
+                                                                       lane * 16),
+                     "r"(w[1])
+                     : "memory");
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_full[slot]);
+        if (++slot == kSfSlots) { slot = 0; sphase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+  } else if (warp >= kFirstEpiWarp) {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - kFirstEpiWarp;
+    const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
+    const int half = ew >> 2;      // which 128 of the 256 columns
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int e, row0, rows;
+      tile_rows(tile, e, row0, rows);
+      const int col0 = (tile % num_n) * BN + half * 128;
+      const int row_in_tile = quarter * 32 + lane;
+      const int row = row0 + row_in_tile;
+      const bool row_ok = row_in_tile < rows && row < p.M_cap;
+      const bool got = mbar_wait(tfull, acc_phase, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(half * 128);
+      uint32_t v0[32], v1[32], v2[32], v3[32];
+      tc_ld32(taddr + 0, v0);
+      tc_ld32(taddr + 32, v1);
+      tc_ld32(taddr + 64, v2);
+      tc_ld32(taddr + 96, v3);
+      tc_wait64(v0, v1);
+      tc_regs_landed(v2);
+      tc_regs_landed(v3);
+      // the accumulator is free for the next tile's MMAs
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+      acc_phase ^= 1u;
+      if (row_ok) {
+        const float wm = p.row_w != nullptr ? p.row_w[row] : 1.0f;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.N + col0);
+        auto put = [&](const uint32_t (&v)[32], int q) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 o;
+            o.x = bf16x2_bits(__uint_as_float(v[8 * i + 0]) * wm, __uint_as_float(v[8 * i + 1]) * wm);
+            o.y = bf16x2_bits(__uint_as_float(v[8 * i + 2]) * wm, __uint_as_float(v[8 * i + 3]) * wm);
+            o.z = bf16x2_bits(__uint_as_float(v[8 * i + 4]) * wm, __uint_as_float(v[8 * i + 5]) * wm);
+            o.w = bf16x2_bits(__uint_as_float(v[8 * i + 6]) * wm, __uint_as_float(v[8 * i + 7]) * wm);
+            dst[q * 4 + i] = o;
+          }
+        };
+        put(v0, 0);
+        put(v1, 1);
+        put(v2, 2);
+        put(v3, 3);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace mx
+}  // namespace
+
+int launch_grouped_gemm_mx(const MxGemmArgs& a, cudaStream_t s) {
+  if (a.E > mx::kMaxE) {
+    set_error("moe_grouped_gemm: block-scaled path supports E <= %d", mx::kMaxE);
+    return MOE_ERR_INVALID_ARG;
+  }
+  CUtensorMap ta, tb;
+  int rc = make_tmap_k128(&ta, a.A, a.Kd, a.M_cap, a.Kd, mx::BM);
+  if (rc != MOE_OK) return rc;
+  rc = make_tmap_k128(&tb, a.W, a.Kd, static_cast<uint64_t>(a.E) * a.N, a.Kd, mx::BN);
+  if (rc != MOE_OK) return rc;
+  mx::Params p;
+  p.a_scale = a.A_scale;
+  p.ld_as = a.ld_as;
+  p.w_scale = a.W_scale;
+  p.start = a.start;
+  p.tile_prefix = a.tile_prefix;
+  p.d_total = a.d_total;
+  p.row_w = a.row_w;
+  p.E = a.E;
+  p.N = a.N;
+  p.Kd = a.Kd;
+  p.M_cap = a.M_cap;
+  p.out = a.out;
+  p.status = a.status;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(mx::grouped_gemm_mx_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, mx::kSmemBytes) != cudaSuccess)
+      return check_launch("cudaFuncSetAttribute(grouped_gemm_mx_kernel)");
+    attr_set[dev] = true;
+  }
+  mx::grouped_gemm_mx_kernel<<<device_sm_count(), mx::kThreads, mx::kSmemBytes, s>>>(ta, tb, p);
+  return check_launch("grouped_gemm_mx_kernel");
+}
+
+}  // namespace moe

@@ -68,6 +68,8 @@ typedef struct CUstream_st* moe_stream_t; /* the same type as cudaStream_t */
 #define MOE_WEIGHT_OUTPUT_ROWS     2 /* ue8m0 path: multiply the down_proj output row by w */
 #define MOE_GEMM_TILE_N128        16 /* tuning: use 128-column GEMM tiles even when N % 256 == 0 */
 #define MOE_GEMM_CTA_PAIR         32 /* tuning: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2) */
+#define MOE_GEMM_PER_KBLOCK_PROMOTION 64 /* ue8m0 scales: promote per K block in registers instead of
+                                            the tensor core's block scaling */
 
 /* Rows per grouped-GEMM tile; tile_prefix counts tiles of this height. */
 #define MOE_BLOCK_M 128
@@ -173,6 +175,11 @@ int moe_expand_scatter(const uint8_t* x, const void* x_scale, int scale_layout, 
  *   start, tile_prefix, d_total: from moe_expand_layout
  *   row_w    device fp32 [M_cap], read only with MOE_WEIGHT_OUTPUT_ROWS
  *   out      device bf16 [M_cap, N]
+ * With MOE_WEIGHT_OUTPUT_ROWS the sum is multiplied by row_w[r] before the
+ * bf16 rounding. With ue8m0 scales and N % 256 == 0 the scales are applied
+ * by the tensor core (kind::mxf8f6f4 block scaling, one accumulator per
+ * tile); otherwise each K block's partial sum is scaled and added in fp32
+ * registers. Both equal the formula up to fp32 summation order.
  * Needs N % 128 == 0, Kd % 128 == 0, E <= 1024.
  */
 int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale_layout, int64_t ld_as,

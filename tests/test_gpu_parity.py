@@ -92,7 +92,7 @@ def test_scatter_bit_exact(mx, cases, name):
         assert np.array_equal(xs[:, :tot], ref["xe_s"][:, :tot])
 
 
-@pytest.mark.parametrize("tile_flag", [0, 16, 32], ids=["default", "bn128", "cta_pair"])
+@pytest.mark.parametrize("tile_flag", [0, 16, 32, 64], ids=["default", "bn128", "cta_pair", "per_kblock"])
 @pytest.mark.parametrize("name", NAMES)
 def test_gate_up_gemm(mx, cases, name, tile_flag):
     c = cases[name]
@@ -139,8 +139,9 @@ def test_act_quant(mx, cases, name):
         assert (bg == br).mean() >= 0.99
 
 
+@pytest.mark.parametrize("promo", [0, 64], ids=["default", "per_kblock"])
 @pytest.mark.parametrize("name", NAMES)
-def test_down_gemm(mx, cases, name):
+def test_down_gemm(mx, cases, name, promo):
     c = cases[name]
     g, ref, M = c["g"], c["ref"], c["M_cap"]
     lay = _gpu_layout(mx, c)
@@ -154,7 +155,7 @@ def test_down_gemm(mx, cases, name):
         di_s = torch.from_numpy(s).cuda()
         flags = mx.MOE_WEIGHT_OUTPUT_ROWS
     row_w = torch.from_numpy(ref["row_w"]).cuda()
-    down = mx.grouped_gemm(di, di_s, c["sl"], lay, g["w2"], g["s2"], row_w=row_w, flags=flags)
+    down = mx.grouped_gemm(di, di_s, c["sl"], lay, g["w2"], g["s2"], row_w=row_w, flags=flags | promo)
     torch.cuda.synchronize()
     tot = ref["total"]
     # ue8m0: the oracle rounds to bf16 before and after the weighting (the
