@@ -306,7 +306,8 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded generator; no dataset or trained weights)",
         "config": {"workload": cfg.name, "T": cfg.T, "n_valid": nv, "H": cfg.H, "I": cfg.I,
                    "E": cfg.E, "top_k": cfg.K, "expert_alignment": cfg.align,
-                   "routing": f"zipf(s={cfg.zipf_s}), {cfg.zipf_zero_experts} experts empty",
+                   "routing": (f"zipf(s={cfg.zipf_s}), {cfg.zipf_zero_experts} experts empty"
+                               if cfg.routing == "zipf" else cfg.routing),
                    "inactive_rows": cfg.inactive_frac, "scales": cfg.scale_mode,
                    "valid_pairs": P, "expanded_rows": M_pad, "M_cap": layer.M_cap,
                    "l2": "flushed between steps (256 MiB write outside the timed events)",

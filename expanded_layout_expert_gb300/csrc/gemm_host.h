@@ -29,6 +29,7 @@ struct MxGemmArgs {
   int64_t M_cap;
   uint16_t* out;
   int32_t* status;
+  unsigned long long* trace;  // optional per-CTA cycle counters
 };
 
 // Launches the tcgen05 block-scaled kernel (N % 256 == 0).

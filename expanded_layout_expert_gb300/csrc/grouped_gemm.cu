@@ -891,6 +891,7 @@ extern "C" int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale
     a.M_cap = M_cap;
     a.out = out;
     a.status = d_status;
+    a.trace = moe::g_trace.load();
     return moe::launch_grouped_gemm_mx(a, reinterpret_cast<cudaStream_t>(stream));
   }
   const bool pair = N % 256 == 0 && (flags & MOE_GEMM_CTA_PAIR) && !(flags & MOE_GEMM_TILE_N128);

@@ -69,7 +69,8 @@ constexpr int kSfOffset = kStages * kStageBytes;
 constexpr int kBarOffset = kSfOffset + kSfSlots * kSfSlotBytes;
 constexpr int kNumBars = 2 * kStages + 2 * kSfSlots + 3;
 constexpr int kMiscOffset = kBarOffset + kNumBars * 8;   // tmem slot, abort flag
-constexpr int kTableOffset = kMiscOffset + 16;           // tile prefix (E+1), start (E)
+constexpr int kTraceOffset = kMiscOffset + 16;           // kTraceWords x u64
+constexpr int kTableOffset = kTraceOffset + 8 * 8;       // tile prefix (E+1), start (E)
 constexpr int kSmemBytes = 1024 + kTableOffset + (2 * kMaxE + 1) * 4;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kSfCol + kSfSlots * kSfSlotCols <= kTmemCols, "TMEM budget");
@@ -86,7 +87,13 @@ struct Params {
   int64_t M_cap;
   uint16_t* out;
   int32_t* status;
+  unsigned long long* trace;  // optional: 8 cycle counters per CTA
 };
+
+// Trace words (cycles, summed per CTA): whole kernel, producer waiting for a
+// free stage, MMA waiting for the accumulator, for operands, for scales,
+// epilogue warp 4 waiting for a finished tile, its work per tile, K blocks.
+constexpr int kTraceWords = 8;
 
 MOE_DEV void drain(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
@@ -100,6 +107,9 @@ MOE_DEV uint32_t bf16x2_bits(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// kTrace: a separate instantiation carries the cycle counters, so the
+// production kernel has none of their code.
+template <bool kTrace>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const Params p) {
@@ -115,11 +125,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* mma_done = tempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOffset + 4);
+  unsigned long long* s_trace = reinterpret_cast<unsigned long long*>(smem + kTraceOffset);
   int* s_tp = reinterpret_cast<int*>(smem + kTableOffset);
   int* s_start = s_tp + (p.E + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  constexpr bool tracing = kTrace;
+  const long long t_kernel0 = tracing ? clock64() : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -134,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(tempty, kEpiWarps);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
+    for (int i = 0; i < kTraceWords; ++i) s_trace[i] = 0ull;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -169,18 +183,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     rows = min(BM, seg_end - row0);
   };
 
+  const int KG = (KB + 3) / 4;  // groups of four K blocks (one packed scale word)
+
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
       int stage = 0, issued = 0;
       uint32_t phase = 0;
+      unsigned long long t_wait = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
         int e, row0, rows;
         tile_rows(tile, e, row0, rows);
         const int n0 = (tile % num_n) * BN;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
+          const long long t0 = tracing ? clock64() : 0;
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (tracing) t_wait += clock64() - t0;
           uint8_t* sa = smem + stage * kStageBytes;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
           tma_load_2d(sa, &tmA, kb * BK, row0, &full[stage]);
@@ -190,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
       }
+      if (tracing) s_trace[1] = t_wait;
       // let the last loads land before the CTA can exit
       const int outstanding = issued < kStages ? issued : kStages;
       for (int i = 1; i <= outstanding; ++i) {
@@ -205,21 +225,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_mx8(BM, BN);
       int stage = 0, slot = 0;
       uint32_t phase = 0, sphase = 0, acc_phase = 0;
+      unsigned long long t_tmem = 0, t_data = 0, t_sf = 0, nkb = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const long long ta = tracing ? clock64() : 0;
         if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, p.status)) break;
+        if (tracing) t_tmem += clock64() - ta;
         tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(kSfCol + slot * kSfSlotCols);
           if ((kb & 3) == 0) {
+            const long long t0 = tracing ? clock64() : 0;
             if (!mbar_wait(&sf_full[slot], sphase, abort_flag, p.status)) { ok = false; break; }
+            if (tracing) t_sf += clock64() - t0;
             tc_fence_after();
             const uint32_t ss = smem_u32(smem + kSfOffset + slot * kSfSlotBytes);
             tc_cp_32x128b_x4(sf_tmem + 0, rows16_desc(ss));
             tc_cp_32x128b_x4(sf_tmem + 4, rows16_desc(ss + kSfBytesA));
             tc_cp_32x128b_x4(sf_tmem + 8, rows16_desc(ss + kSfBytesA + 512));
           }
+          const long long t1 = tracing ? clock64() : 0;
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          if (tracing) {
+            t_data += clock64() - t1;
+            ++nkb;
+          }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
@@ -240,6 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(tfull);
         acc_phase ^= 1u;
       }
+      if (tracing) {
+        s_trace[2] = t_tmem;
+        s_trace[3] = t_data;
+        s_trace[4] = t_sf;
+        s_trace[7] = nkb;
+      }
       // every MMA issued so far must complete before TMEM is released
       tc_commit(mma_done);
       drain(mma_done, 0);
@@ -248,7 +284,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- scale loader
     int slot = 0;
     uint32_t sphase = 0;
-    const int KG = (KB + 3) / 4;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       int e, row0, rows;
       tile_rows(tile, e, row0, rows);
@@ -297,15 +332,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
     const int half = ew >> 2;      // which 128 of the 256 columns
     uint32_t acc_phase = 0;
+    unsigned long long t_ewait = 0, t_ework = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       int e, row0, rows;
       tile_rows(tile, e, row0, rows);
       const int col0 = (tile % num_n) * BN + half * 128;
+      const long long t0 = tracing ? clock64() : 0;
       const int row_in_tile = quarter * 32 + lane;
       const int row = row0 + row_in_tile;
       const bool row_ok = row_in_tile < rows && row < p.M_cap;
       const bool got = mbar_wait(tfull, acc_phase, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, got)) break;
+      const long long t1 = tracing ? clock64() : 0;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(half * 128);
@@ -341,6 +379,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         put(v2, 2);
         put(v3, 3);
       }
+      if (tracing) {
+        const long long t2 = clock64();
+        t_ewait += t1 - t0;
+        t_ework += t2 - t1;
+      }
+    }
+    if (tracing && ew == 0 && lane == 0) {
+      s_trace[5] = t_ewait;
+      s_trace[6] = t_ework;
     }
   }
 
@@ -349,6 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (tracing && threadIdx.x == 0) {
+    s_trace[0] = static_cast<unsigned long long>(clock64() - t_kernel0);
+    for (int i = 0; i < kTraceWords; ++i) p.trace[blockIdx.x * kTraceWords + i] = s_trace[i];
   }
 }
 
@@ -379,16 +430,19 @@ int launch_grouped_gemm_mx(const MxGemmArgs& a, cudaStream_t s) {
   p.M_cap = a.M_cap;
   p.out = a.out;
   p.status = a.status;
-  static bool attr_set[64] = {};
+  p.trace = a.trace;
+  static bool attr_set[2][64] = {};
+  const bool trace = p.trace != nullptr;
+  auto kernel = trace ? mx::grouped_gemm_mx_kernel<true> : mx::grouped_gemm_mx_kernel<false>;
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(mx::grouped_gemm_mx_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, mx::kSmemBytes) != cudaSuccess)
+  if (dev >= 0 && dev < 64 && !attr_set[trace][dev]) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             mx::kSmemBytes) != cudaSuccess)
       return check_launch("cudaFuncSetAttribute(grouped_gemm_mx_kernel)");
-    attr_set[dev] = true;
+    attr_set[trace][dev] = true;
   }
-  mx::grouped_gemm_mx_kernel<<<device_sm_count(), mx::kThreads, mx::kSmemBytes, s>>>(ta, tb, p);
+  kernel<<<device_sm_count(), mx::kThreads, mx::kSmemBytes, s>>>(ta, tb, p);
   return check_launch("grouped_gemm_mx_kernel");
 }
 
