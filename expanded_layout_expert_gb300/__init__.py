@@ -14,17 +14,19 @@ from typing import Optional
 import torch
 
 from . import _capi
-from ._capi import (MOE_BLOCK_M, MOE_FOLD_WEIGHT_INTO_SCALE, MOE_GEMM_CTA_PAIR, MOE_GEMM_PER_KBLOCK_PROMOTION,
+from ._capi import (MOE_BLOCK_M, MOE_FFN_UNFUSED, MOE_FOLD_WEIGHT_INTO_SCALE, MOE_GEMM_CTA_PAIR,
+                    MOE_GEMM_PER_KBLOCK_PROMOTION,
                     MOE_GEMM_TILE_N128,
                     MOE_SCALE_F32_ROWMAJOR, MOE_SCALE_UE8M0_PACKED_COLMAJOR,
                     MOE_WEIGHT_OUTPUT_ROWS, MoEError, check, load)
 
 __all__ = [
     "expanded_capacity", "workspace_size", "expand_layout", "expand_scatter", "grouped_gemm",
-    "act_quant", "grouped_ffn", "combine", "ExpandedMoELayer", "Layout", "MoEError",
+    "act_quant", "grouped_gemm_act_quant", "grouped_ffn", "combine", "ExpandedMoELayer", "Layout",
+    "MoEError",
     "MOE_SCALE_F32_ROWMAJOR", "MOE_SCALE_UE8M0_PACKED_COLMAJOR", "MOE_FOLD_WEIGHT_INTO_SCALE",
     "MOE_WEIGHT_OUTPUT_ROWS", "MOE_GEMM_TILE_N128", "MOE_GEMM_CTA_PAIR",
-    "MOE_GEMM_PER_KBLOCK_PROMOTION", "MOE_BLOCK_M",
+    "MOE_GEMM_PER_KBLOCK_PROMOTION", "MOE_FFN_UNFUSED", "MOE_BLOCK_M",
     "scale_layout_of",
 ]
 
@@ -157,6 +159,27 @@ def act_quant(gu: torch.Tensor, row_w: Optional[torch.Tensor], flags: int, scale
     return di, di_scale
 
 
+def grouped_gemm_act_quant(A: torch.Tensor, A_scale: torch.Tensor, scale_layout: int, lay: Layout,
+                           W13: torch.Tensor, W13_scale: torch.Tensor, flags: int = 0,
+                           di: Optional[torch.Tensor] = None, di_scale: Optional[torch.Tensor] = None,
+                           status: Optional[torch.Tensor] = None, stream=None):
+    """gate_up GEMM with silu*mul and the fp8 quantiser fused (ue8m0 scales)."""
+    M_cap, H = A.shape
+    E, twoI, _ = W13.shape
+    I = twoI // 2
+    if di is None:
+        di = torch.zeros(M_cap, I, dtype=torch.uint8, device=A.device)
+    if di_scale is None:
+        di_scale = new_scale(M_cap, I // 128, scale_layout, A.device)
+    rc = load().moe_grouped_gemm_act_quant(_ptr(A), _ptr(A_scale), scale_layout, A_scale.shape[1],
+                                           _ptr(lay.start), _ptr(lay.tile_prefix), _ptr(lay.total),
+                                           _ptr(W13), _ptr(W13_scale), None, flags, E, I, H, M_cap,
+                                           _ptr(di), _ptr(di_scale), di_scale.shape[1], _ptr(status),
+                                           _stream(stream))
+    check(rc, "moe_grouped_gemm_act_quant")
+    return di, di_scale
+
+
 def grouped_ffn(xe, xe_scale, scale_layout: int, lay: Layout, w13, s13, w2, s2, row_w, flags: int,
                 gateup=None, down_in=None, down_in_scale=None, down_out=None, status=None,
                 stream=None):
@@ -267,6 +290,9 @@ class ExpandedMoELayer:
                             self.H, self.K, _ptr(self.y), s), "moe_combine")
         return self.y
 
-    # number of kernels one forward launches (layout 2, scatter 1, GEMM 2,
-    # act+quant 1, combine 1)
-    KERNELS_PER_FORWARD = 7
+    @property
+    def kernels_per_forward(self) -> int:
+        """Kernels one forward launches: layout 2, scatter 1, combine 1, and
+        gate_up + act+quant + down (3), or 2 where gate_up carries act+quant
+        (ue8m0 scales)."""
+        return 4 + (2 if self.scale_mode == "ue8m0" else 3)

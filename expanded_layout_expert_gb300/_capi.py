@@ -27,6 +27,7 @@ MOE_WEIGHT_OUTPUT_ROWS = 2
 MOE_GEMM_TILE_N128 = 16
 MOE_GEMM_CTA_PAIR = 32
 MOE_GEMM_PER_KBLOCK_PROMOTION = 64
+MOE_FFN_UNFUSED = 128
 
 MOE_BLOCK_M = 128
 
@@ -51,6 +52,8 @@ SIGNATURES = {
                                  P, P, I64, P, P, P]),
     "moe_grouped_gemm": (I32, [P, P, I32, I64, P, P, P, P, P, P, I32, I32, I32, I32, I64, P, P, P]),
     "moe_act_quant": (I32, [P, I32, P, I32, I32, P, I64, P, P, I64, P, P]),
+    "moe_grouped_gemm_act_quant": (I32, [P, P, I32, I64, P, P, P, P, P, P, I32, I32, I32, I32, I64,
+                                         P, P, I64, P, P]),
     "moe_grouped_ffn": (I32, [P, P, I64, I32, P, P, P, P, P, P, P, P, I32, I32, I32, I32, I64,
                               P, P, P, I64, P, P, P]),
     "moe_combine": (I32, [P, P, P, P, I64, I32, I32, P, P]),

@@ -11,9 +11,7 @@
 // in each 256-column half, so every load and store instruction of the warp
 // is one contiguous, fully coalesced run. HBM-bound: 4I bytes read and
 // I + scales written per row.
-#include <cuda_bf16.h>
-#include <cuda_fp8.h>
-
+#include "act_quant.cuh"
 #include "common.cuh"
 #include "host_util.h"
 
@@ -21,20 +19,6 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-
-MOE_DEV uint32_t ue8m0_round_up(float s) {
-  const uint32_t bits = __float_as_uint(s);
-  uint32_t ex = (bits >> 23) & 0xFFu;
-  const uint32_t man = bits & 0x7FFFFFu;
-  if (man != 0u && ex != 0xFEu && !(ex == 0u && man <= 0x400000u)) ex += 1u;
-  return ex & 0xFFu;
-}
-
-// 2^(127-b) for an exponent byte b, as fp32 (2^-127 is the subnormal 0x00400000).
-MOE_DEV float pow2_inverse(uint32_t b) {
-  if (b <= 253u) return __uint_as_float((254u - b) << 23);
-  return b == 254u ? __uint_as_float(0x00400000u) : __uint_as_float(0x00200000u);
-}
 
 // 8 bf16 gate + 8 bf16 up -> 8 bf16-rounded silu(g)*u values.
 MOE_DEV void silu_mul8(const uint4& g, const uint4& u, float (&h)[8]) {
@@ -44,24 +28,9 @@ MOE_DEV void silu_mul8(const uint4& g, const uint4& u, float (&h)[8]) {
   for (int i = 0; i < 4; ++i) {
     const float2 gf = __bfloat1622float2(g2[i]);
     const float2 uf = __bfloat1622float2(u2[i]);
-    // silu in fast fp32 (the value is rounded to bf16 next): g / (1 + e^-g)
-    const float a = __fmul_rn(__fdividef(gf.x, __fadd_rn(1.0f, __expf(-gf.x))), uf.x);
-    const float b = __fmul_rn(__fdividef(gf.y, __fadd_rn(1.0f, __expf(-gf.y))), uf.y);
-    h[2 * i] = __bfloat162float(__float2bfloat16_rn(a));
-    h[2 * i + 1] = __bfloat162float(__float2bfloat16_rn(b));
+    h[2 * i] = silu_mul_bf16(gf.x, uf.x);
+    h[2 * i + 1] = silu_mul_bf16(gf.y, uf.y);
   }
-}
-
-// 8 values times the inverse scale -> 8 e4m3 codes (round to nearest even,
-// saturating to +-448).
-MOE_DEV uint2 quant8(const float (&h)[8], float inv) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 v = make_float2(__fmul_rn(h[2 * i], inv), __fmul_rn(h[2 * i + 1], inv));
-    w[i] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
-  }
-  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(
@@ -104,27 +73,16 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(
       m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
       m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
     }
-    m0 = fmaxf(m0, 1e-10f);
-    m1 = fmaxf(m1, 1e-10f);
     // stored scale amax/448; codes h * (448/amax), as the pages' quantiser
-    // (_situ_mul_quant_contig_kernel) computes them
-    const float s0 = __fdiv_rn(m0, 448.0f);
-    const float s1 = __fdiv_rn(m1, 448.0f);
-    uint32_t b0 = 0, b1 = 0;
-    float inv0, inv1;
-    if (ue8m0) {
-      // power-of-two scale 2^(b-127); its inverse 2^(127-b) is exact
-      b0 = ue8m0_round_up(s0);
-      b1 = ue8m0_round_up(s1);
-      inv0 = pow2_inverse(b0);
-      inv1 = pow2_inverse(b1);
-    } else {
-      inv0 = __fdiv_rn(448.0f, m0);
-      inv1 = __fdiv_rn(448.0f, m1);
-    }
+    // (_situ_mul_quant_contig_kernel) computes them; ue8m0: the scale rounded
+    // up to a power of two, whose inverse is exact
+    float s0, s1, inv0, inv1;
+    uint32_t b0, b1;
+    group_scale(m0, ue8m0 != 0, s0, inv0, b0);
+    group_scale(m1, ue8m0 != 0, s1, inv1, b1);
     uint8_t* out = di + r * I;
-    if (a0) *reinterpret_cast<uint2*>(out + c0) = quant8(h0, inv0);
-    if (a1) *reinterpret_cast<uint2*>(out + c1) = quant8(h1, inv1);
+    if (a0) *reinterpret_cast<uint2*>(out + c0) = fp8x8(h0, inv0);
+    if (a1) *reinterpret_cast<uint2*>(out + c1) = fp8x8(h1, inv1);
 
     const int half_lane = lane & 15;
     const int g0 = q * 4 + (lane >> 4);

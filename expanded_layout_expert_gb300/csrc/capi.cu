@@ -89,15 +89,29 @@ int moe_grouped_ffn(const uint8_t* xe, const void* xe_scale, int64_t ld_xes, int
               "moe_grouped_ffn: choose one weighting flag");
   MOE_REQUIRE(!(flags & MOE_FOLD_WEIGHT_INTO_SCALE) || scale_layout == MOE_SCALE_F32_ROWMAJOR,
               "moe_grouped_ffn: the fold needs fp32 scales (a power-of-two scale cannot absorb a weight)");
-  int rc = moe_grouped_gemm(xe, xe_scale, scale_layout, ld_xes, start, tile_prefix, d_total, w13,
-                            s13, nullptr, 0, E, 2 * I, H, M_cap, gateup_ws, d_status, stream);
-  if (rc != MOE_OK) return rc;
-  rc = moe_act_quant(gateup_ws, I, row_w, flags & MOE_FOLD_WEIGHT_INTO_SCALE, scale_layout,
-                     d_total, M_cap, down_in, down_in_scale, ld_dis, d_status, stream);
-  if (rc != MOE_OK) return rc;
+  int rc;
+  const bool fused = scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR &&
+                     !(flags & (MOE_FFN_UNFUSED | MOE_GEMM_PER_KBLOCK_PROMOTION));
+  if (fused) {
+    // gate_up with silu*mul and the quantiser in its epilogue: gateup_ws unused
+    rc = moe_grouped_gemm_act_quant(xe, xe_scale, scale_layout, ld_xes, start, tile_prefix,
+                                    d_total, w13, s13, row_w, 0, E, I, H, M_cap, down_in,
+                                    down_in_scale, ld_dis, d_status, stream);
+    if (rc != MOE_OK) return rc;
+  } else {
+    MOE_REQUIRE(gateup_ws, "moe_grouped_ffn: null gateup_ws");
+    const int gflags = flags & MOE_GEMM_PER_KBLOCK_PROMOTION;
+    rc = moe_grouped_gemm(xe, xe_scale, scale_layout, ld_xes, start, tile_prefix, d_total, w13,
+                          s13, nullptr, gflags, E, 2 * I, H, M_cap, gateup_ws, d_status, stream);
+    if (rc != MOE_OK) return rc;
+    rc = moe_act_quant(gateup_ws, I, row_w, flags & MOE_FOLD_WEIGHT_INTO_SCALE, scale_layout,
+                       d_total, M_cap, down_in, down_in_scale, ld_dis, d_status, stream);
+    if (rc != MOE_OK) return rc;
+  }
   return moe_grouped_gemm(down_in, down_in_scale, scale_layout, ld_dis, start, tile_prefix,
-                          d_total, w2, s2, row_w, flags & MOE_WEIGHT_OUTPUT_ROWS, E, H, I, M_cap,
-                          down_out, d_status, stream);
+                          d_total, w2, s2, row_w,
+                          flags & (MOE_WEIGHT_OUTPUT_ROWS | MOE_GEMM_PER_KBLOCK_PROMOTION), E, H, I,
+                          M_cap, down_out, d_status, stream);
 }
 
 }  // extern "C"

@@ -30,6 +30,13 @@ struct MxGemmArgs {
   uint16_t* out;
   int32_t* status;
   unsigned long long* trace;  // optional per-CTA cycle counters
+  // Non-null: W is W13 [E, N = 2I, Kd] and the kernel applies silu(gate)*up
+  // and the ue8m0 fp8 quantiser in its epilogue, writing down_proj's input
+  // di [M_cap, I] and its packed scales (int32 words [ceil(I/512), ld_ds],
+  // addressed as bytes) instead of `out`.
+  uint8_t* di = nullptr;
+  uint8_t* di_scale = nullptr;
+  int64_t ld_ds = 0;
 };
 
 // Launches the tcgen05 block-scaled kernel (N % 256 == 0).

@@ -927,3 +927,53 @@ extern "C" int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale
     return staged ? moe::launch<256, true>(ta, tb, prm, s) : moe::launch<256, false>(ta, tb, prm, s);
   return staged ? moe::launch<128, true>(ta, tb, prm, s) : moe::launch<128, false>(ta, tb, prm, s);
 }
+
+extern "C" int moe_grouped_gemm_act_quant(const uint8_t* A, const void* A_scale, int scale_layout,
+                                          int64_t ld_as, const int32_t* start,
+                                          const int32_t* tile_prefix, const int32_t* d_total,
+                                          const uint8_t* W13, const void* W13_scale,
+                                          const float* row_w, int flags, int E, int I, int H,
+                                          int64_t M_cap, uint8_t* di, void* di_scale,
+                                          int64_t ld_ds, int32_t* d_status, moe_stream_t stream) {
+  MOE_REQUIRE(A && A_scale && start && tile_prefix && d_total && W13 && W13_scale && di && di_scale,
+              "moe_grouped_gemm_act_quant: null pointer");
+  MOE_REQUIRE(E > 0 && E <= moe::kMaxE, "moe_grouped_gemm_act_quant: E must be in [1, 1024]");
+  MOE_REQUIRE(I > 0 && I % 128 == 0 && H > 0 && H % 128 == 0,
+              "moe_grouped_gemm_act_quant: I and H must be positive multiples of 128");
+  MOE_REQUIRE(M_cap > 0 && M_cap <= INT32_MAX && static_cast<int64_t>(E) * 2 * I <= INT32_MAX,
+              "moe_grouped_gemm_act_quant: sizes exceed int32");
+  if (scale_layout != MOE_SCALE_UE8M0_PACKED_COLMAJOR) {
+    moe::set_error("moe_grouped_gemm_act_quant: the fused path takes ue8m0 scales");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  MOE_REQUIRE(!(flags & MOE_FOLD_WEIGHT_INTO_SCALE),
+              "moe_grouped_gemm_act_quant: a power-of-two scale cannot absorb the weight");
+  MOE_REQUIRE(ld_as >= M_cap && ld_ds >= M_cap,
+              "moe_grouped_gemm_act_quant: packed scale leading dimension < M_cap");
+  MOE_REQUIRE(moe::aligned(A, 16) && moe::aligned(W13, 16) && moe::aligned(di, 16) &&
+                  moe::aligned(di_scale, 4),
+              "moe_grouped_gemm_act_quant: A, W13 and di must be 16-byte aligned");
+  MOE_REQUIRE_DEVICE();
+  (void)row_w;
+  moe::MxGemmArgs a;
+  a.A = A;
+  a.A_scale = static_cast<const uint32_t*>(A_scale);
+  a.ld_as = ld_as;
+  a.start = start;
+  a.tile_prefix = tile_prefix;
+  a.d_total = d_total;
+  a.W = W13;
+  a.W_scale = static_cast<const uint8_t*>(W13_scale);
+  a.row_w = nullptr;
+  a.E = E;
+  a.N = 2 * I;
+  a.Kd = H;
+  a.M_cap = M_cap;
+  a.out = nullptr;
+  a.status = d_status;
+  a.trace = moe::g_trace.load();
+  a.di = di;
+  a.di_scale = static_cast<uint8_t*>(di_scale);
+  a.ld_ds = ld_ds;
+  return moe::launch_grouped_gemm_mx(a, reinterpret_cast<cudaStream_t>(stream));
+}

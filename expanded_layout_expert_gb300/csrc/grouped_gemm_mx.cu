@@ -36,6 +36,7 @@
 // (A: 4 columns, B: 8 columns).
 #include <cuda_bf16.h>
 
+#include "act_quant.cuh"
 #include "common.cuh"
 #include "gemm_host.h"
 #include "host_util.h"
@@ -67,10 +68,11 @@ constexpr int kSfSlotCols = 16;
 
 constexpr int kSfOffset = kStages * kStageBytes;
 constexpr int kBarOffset = kSfOffset + kSfSlots * kSfSlotBytes;
-constexpr int kNumBars = 2 * kStages + 2 * kSfSlots + 3;
+constexpr int kNumBars = 2 * kStages + 2 * kSfSlots + 3 + 4;  // + 4 amax exchanges
 constexpr int kMiscOffset = kBarOffset + kNumBars * 8;   // tmem slot, abort flag
 constexpr int kTraceOffset = kMiscOffset + 16;           // kTraceWords x u64
-constexpr int kTableOffset = kTraceOffset + 8 * 8;       // tile prefix (E+1), start (E)
+constexpr int kAmaxOffset = kTraceOffset + 8 * 8;        // fused: [2 tiles][2 halves][128 rows] f32
+constexpr int kTableOffset = kAmaxOffset + 2 * 2 * 128 * 4;  // tile prefix (E+1), start (E)
 constexpr int kSmemBytes = 1024 + kTableOffset + (2 * kMaxE + 1) * 4;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kSfCol + kSfSlots * kSfSlotCols <= kTmemCols, "TMEM budget");
@@ -88,6 +90,11 @@ struct Params {
   uint16_t* out;
   int32_t* status;
   unsigned long long* trace;  // optional: 8 cycle counters per CTA
+  // fused gate_up + act+quant: down_proj's input codes [M_cap, N/2] and
+  // packed ue8m0 scales (bytes of int32 words [ceil(N/256/4), ld_ds])
+  uint8_t* di;
+  uint8_t* di_scale;
+  int64_t ld_ds;
 };
 
 // Trace words (cycles, summed per CTA): whole kernel, producer waiting for a
@@ -109,7 +116,17 @@ MOE_DEV uint32_t bf16x2_bits(float a, float b) {
 
 // kTrace: a separate instantiation carries the cycle counters, so the
 // production kernel has none of their code.
-template <bool kTrace>
+// kFused: gate_up with silu(gate)*up and the fp8 quantiser of down_proj's
+// input in the epilogue (W = W13 [E, 2I, H]). A tile is 128 rows x 128
+// intermediate columns t*128..: its B tile stacks W13's gate rows
+// [t*128, +128) over its up rows [I + t*128, +128), so every output group of
+// 128 sits in one accumulator (gate in columns 0-127, up in 128-255). The
+// two epilogue warps of a lane quarter take 64 columns each, exchange their
+// row maxima through shared memory, and write the codes and the group's
+// scale byte; gate_up's bf16 output never goes to memory. The arithmetic is
+// the stand-alone kernels' (bf16 rounding of the GEMM output, then the
+// shared act+quant math), so the codes and scales are the same bit for bit.
+template <bool kTrace, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const Params p) {
@@ -123,6 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = sf_empty + kSfSlots;
   uint64_t* tempty = tfull + 1;
   uint64_t* mma_done = tempty + 1;
+  uint64_t* amax_bar = mma_done + 1;  // [4], one per TMEM lane quarter
+  float* s_amax = reinterpret_cast<float*>(smem + kAmaxOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOffset + 4);
   unsigned long long* s_trace = reinterpret_cast<unsigned long long*>(smem + kTraceOffset);
@@ -146,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(tfull, 1);
     mbar_init(tempty, kEpiWarps);
     mbar_init(mma_done, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&amax_bar[q], 64);  // both warps of the quarter
     *abort_flag = 0;
     for (int i = 0; i < kTraceWords; ++i) s_trace[i] = 0ull;
     fence_mbar_init();
@@ -165,7 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int total = *p.d_total;
   if (total > p.M_cap) total = static_cast<int>(p.M_cap);
-  const int num_n = p.N / BN;
+  // tiles per m block: 256 output columns, or (fused) 128 intermediate columns
+  const int num_n = kFused ? p.N / 256 : p.N / BN;
+  const int I = p.N / 2;
   const int num_tiles = s_tp[p.E] * num_n;
   const int KB = p.Kd / BK;
   const int NB = p.N / 128;
@@ -203,7 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + stage * kStageBytes;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
           tma_load_2d(sa, &tmA, kb * BK, row0, &full[stage]);
-          tma_load_2d(sa + kABytes, &tmB, kb * BK, e * p.N + n0, &full[stage]);
+          if (kFused) {
+            const int t = tile % num_n;
+            tma_load_2d(sa + kABytes, &tmB, kb * BK, e * p.N + t * 128, &full[stage]);
+            tma_load_2d(sa + kABytes + kBBytes / 2, &tmB, kb * BK, e * p.N + I + t * 128,
+                        &full[stage]);
+          } else {
+            tma_load_2d(sa + kABytes, &tmB, kb * BK, e * p.N + n0, &full[stage]);
+          }
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -287,7 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       int e, row0, rows;
       tile_rows(tile, e, row0, rows);
-      const int nb0 = (tile % num_n) * (BN / 128);
+      // weight-scale blocks of the B tile's two 128-row halves
+      const int nbh0 = kFused ? tile % num_n : (tile % num_n) * 2;
+      const int nbh1 = kFused ? I / 128 + tile % num_n : nbh0 + 1;
       bool ok = true;
       for (int g = 0; g < KG; ++g) {
         const bool got = mbar_wait(&sf_empty[slot], sphase ^ 1u, abort_flag, p.status);
@@ -301,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint8_t* ws = p.w_scale + (static_cast<int64_t>(e) * NB + nb0 + h) * KB + 4 * g;
+          const uint8_t* ws =
+              p.w_scale + (static_cast<int64_t>(e) * NB + (h ? nbh1 : nbh0)) * KB + 4 * g;
           uint32_t word = 0;
 #pragma unroll
           for (int b = 0; b < 4; ++b)
@@ -333,10 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = ew >> 2;      // which 128 of the 256 columns
     uint32_t acc_phase = 0;
     unsigned long long t_ewait = 0, t_ework = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    int iter = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++iter) {
       int e, row0, rows;
       tile_rows(tile, e, row0, rows);
-      const int col0 = (tile % num_n) * BN + half * 128;
       const long long t0 = tracing ? clock64() : 0;
       const int row_in_tile = quarter * 32 + lane;
       const int row = row0 + row_in_tile;
@@ -345,13 +377,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       const long long t1 = tracing ? clock64() : 0;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                             static_cast<uint32_t>(half * 128);
+      const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+      // stand-alone: columns [128 half, +128); fused: gate [64 half, +64)
+      // and up [128 + 64 half, +64)
+      const uint32_t c_lo = kFused ? static_cast<uint32_t>(64 * half) : static_cast<uint32_t>(128 * half);
+      const uint32_t c_hi = kFused ? static_cast<uint32_t>(128 + 64 * half) : c_lo + 64u;
       uint32_t v0[32], v1[32], v2[32], v3[32];
-      tc_ld32(taddr + 0, v0);
-      tc_ld32(taddr + 32, v1);
-      tc_ld32(taddr + 64, v2);
-      tc_ld32(taddr + 96, v3);
+      tc_ld32(tq + c_lo, v0);
+      tc_ld32(tq + c_lo + 32, v1);
+      tc_ld32(tq + c_hi, v2);
+      tc_ld32(tq + c_hi + 32, v3);
       tc_wait64(v0, v1);
       tc_regs_landed(v2);
       tc_regs_landed(v3);
@@ -360,7 +395,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty);
       acc_phase ^= 1u;
-      if (row_ok) {
+      if constexpr (kFused) {
+        // h = bf16(silu(bf16 g) * bf16 u), kept in v0/v1; this half's row max
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float h0 = silu_mul_bf16(bf16_round(__uint_as_float(v0[j])),
+                                         bf16_round(__uint_as_float(v2[j])));
+          const float h1 = silu_mul_bf16(bf16_round(__uint_as_float(v1[j])),
+                                         bf16_round(__uint_as_float(v3[j])));
+          v0[j] = __float_as_uint(h0);
+          v1[j] = __float_as_uint(h1);
+          m = fmaxf(m, fmaxf(fabsf(h0), fabsf(h1)));
+        }
+        // the other half's maximum for the same row (double-buffered by tile)
+        const int par = iter & 1;
+        s_amax[(par * 2 + half) * 128 + row_in_tile] = m;
+        mbar_arrive(&amax_bar[quarter]);
+        const bool got2 = mbar_wait(&amax_bar[quarter], static_cast<uint32_t>(par), abort_flag,
+                                    p.status);
+        if (!__all_sync(0xffffffffu, got2)) break;
+        const float amax = fmaxf(m, s_amax[(par * 2 + (half ^ 1)) * 128 + row_in_tile]);
+        float sc, inv;
+        uint32_t b;
+        group_scale(amax, true, sc, inv, b);
+        if (row_ok) {
+          const int t = tile % num_n;
+          uint4* dst = reinterpret_cast<uint4*>(p.di + static_cast<int64_t>(row) * I + t * 128 +
+                                                half * 64);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            float h[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) h[j] = __uint_as_float(v0[16 * q + j]);
+            const uint2 lo = fp8x8(h, inv), hi = fp8x8(h + 8, inv);
+            dst[q] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          }
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            float h[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) h[j] = __uint_as_float(v1[16 * q + j]);
+            const uint2 lo = fp8x8(h, inv), hi = fp8x8(h + 8, inv);
+            dst[2 + q] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          }
+          if (half == 0) {
+            // byte t%4 of word (t/4, row); the last group also clears the
+            // word's unused bytes
+            uint8_t* w = p.di_scale + (static_cast<int64_t>(t >> 2) * p.ld_ds + row) * 4;
+            w[t & 3] = static_cast<uint8_t>(b);
+            if (t == num_n - 1)
+              for (int z = (t & 3) + 1; z < 4; ++z) w[z] = 0;
+          }
+        }
+      } else if (row_ok) {
+        const int col0 = (tile % num_n) * BN + half * 128;
         const float wm = p.row_w != nullptr ? p.row_w[row] : 1.0f;
         uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.N + col0);
         auto put = [&](const uint32_t (&v)[32], int q) {
@@ -414,7 +503,9 @@ int launch_grouped_gemm_mx(const MxGemmArgs& a, cudaStream_t s) {
   CUtensorMap ta, tb;
   int rc = make_tmap_k128(&ta, a.A, a.Kd, a.M_cap, a.Kd, mx::BM);
   if (rc != MOE_OK) return rc;
-  rc = make_tmap_k128(&tb, a.W, a.Kd, static_cast<uint64_t>(a.E) * a.N, a.Kd, mx::BN);
+  const bool fused = a.di != nullptr;
+  rc = make_tmap_k128(&tb, a.W, a.Kd, static_cast<uint64_t>(a.E) * a.N, a.Kd,
+                      fused ? mx::BN / 2 : mx::BN);
   if (rc != MOE_OK) return rc;
   mx::Params p;
   p.a_scale = a.A_scale;
@@ -431,16 +522,22 @@ int launch_grouped_gemm_mx(const MxGemmArgs& a, cudaStream_t s) {
   p.out = a.out;
   p.status = a.status;
   p.trace = a.trace;
-  static bool attr_set[2][64] = {};
+  p.di = a.di;
+  p.di_scale = a.di_scale;
+  p.ld_ds = a.ld_ds;
+  static bool attr_set[4][64] = {};
   const bool trace = p.trace != nullptr;
-  auto kernel = trace ? mx::grouped_gemm_mx_kernel<true> : mx::grouped_gemm_mx_kernel<false>;
+  void (*kernel)(CUtensorMap, CUtensorMap, mx::Params) =
+      fused ? (trace ? mx::grouped_gemm_mx_kernel<true, true> : mx::grouped_gemm_mx_kernel<false, true>)
+            : (trace ? mx::grouped_gemm_mx_kernel<true, false> : mx::grouped_gemm_mx_kernel<false, false>);
+  const int variant = (fused ? 2 : 0) + (trace ? 1 : 0);
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[trace][dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[variant][dev]) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              mx::kSmemBytes) != cudaSuccess)
       return check_launch("cudaFuncSetAttribute(grouped_gemm_mx_kernel)");
-    attr_set[trace][dev] = true;
+    attr_set[variant][dev] = true;
   }
   kernel<<<device_sm_count(), mx::kThreads, mx::kSmemBytes, s>>>(ta, tb, p);
   return check_launch("grouped_gemm_mx_kernel");

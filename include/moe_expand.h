@@ -70,6 +70,7 @@ typedef struct CUstream_st* moe_stream_t; /* the same type as cudaStream_t */
 #define MOE_GEMM_CTA_PAIR         32 /* tuning: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2) */
 #define MOE_GEMM_PER_KBLOCK_PROMOTION 64 /* ue8m0 scales: promote per K block in registers instead of
                                             the tensor core's block scaling */
+#define MOE_FFN_UNFUSED          128 /* moe_grouped_ffn: gate_up, act+quant and down as three launches */
 
 /* Rows per grouped-GEMM tile; tile_prefix counts tiles of this height. */
 #define MOE_BLOCK_M 128
@@ -204,6 +205,28 @@ int moe_act_quant(const uint16_t* gu, int I, const float* row_w, int flags, int 
                   int64_t ld_ds, int32_t* d_status, moe_stream_t stream);
 
 /*
+ * gate_up GEMM with silu(gate)*up and the fp8 quantiser of down_proj's input
+ * in its epilogue: the result equals moe_grouped_gemm into a bf16 [M_cap, 2I]
+ * buffer followed by moe_act_quant, bit for bit, without that buffer going
+ * through memory (the fusion the pages' _situ_mul_quant_contig_kernel makes of
+ * silu_and_mul and the group quant, here taken into the GEMM itself).
+ *   A, A_scale, ld_as, start, tile_prefix, d_total: as moe_grouped_gemm
+ *   W13      device uint8 [E, 2I, H]: gate rows [0, I), up rows [I, 2I)
+ *   di       device uint8 [M_cap, I], 16-byte aligned; rows r < *d_total written
+ *   di_scale packed ue8m0 int32 [ceil(I/512), ld_ds], ld_ds >= M_cap
+ * Takes scale_layout MOE_SCALE_UE8M0_PACKED_COLMAJOR (the tensor core applies
+ * the power-of-two scales); returns MOE_ERR_UNSUPPORTED for fp32 scales, whose
+ * callers use the two-launch path. row_w is unused (a power-of-two scale
+ * cannot absorb the weight; weight down_proj's output rows instead).
+ */
+int moe_grouped_gemm_act_quant(const uint8_t* A, const void* A_scale, int scale_layout,
+                               int64_t ld_as, const int32_t* start, const int32_t* tile_prefix,
+                               const int32_t* d_total, const uint8_t* W13, const void* W13_scale,
+                               const float* row_w, int flags, int E, int I, int H, int64_t M_cap,
+                               uint8_t* di, void* di_scale, int64_t ld_ds, int32_t* d_status,
+                               moe_stream_t stream);
+
+/*
  * The expert FFN over the expanded rows: moe_grouped_gemm with W13 [E, 2I, H]
  * into gateup_ws bf16 [M_cap, 2I], moe_act_quant into down_in uint8
  * [M_cap, I] / down_in_scale (ld_dis), moe_grouped_gemm with W2 [E, H, I]
@@ -211,6 +234,9 @@ int moe_act_quant(const uint16_t* gu, int I, const float* row_w, int flags, int 
  * flags: MOE_FOLD_WEIGHT_INTO_SCALE (fp32 scales) or MOE_WEIGHT_OUTPUT_ROWS
  * (ue8m0 scales; a power-of-two scale cannot absorb the weight, so the output
  * row is weighted instead), or 0 (unweighted; moe_combine may weight).
+ * With ue8m0 scales the first two steps run as one launch
+ * (moe_grouped_gemm_act_quant) and gateup_ws is not touched (it may be NULL);
+ * MOE_FFN_UNFUSED or MOE_GEMM_PER_KBLOCK_PROMOTION keep three launches.
  */
 int moe_grouped_ffn(const uint8_t* xe, const void* xe_scale, int64_t ld_xes, int scale_layout,
                     const int32_t* start, const int32_t* tile_prefix, const int32_t* d_total,

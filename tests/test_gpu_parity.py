@@ -109,6 +109,53 @@ def test_gate_up_gemm(mx, cases, name, tile_flag):
     assert (u16(gu)[tot:] == 0).all(), "rows past the total must be untouched"
 
 
+UE8M0_NAMES = [c.name for c in synth.PARITY_CONFIGS if c.scale_mode == "ue8m0"]
+
+
+@pytest.mark.parametrize("name", UE8M0_NAMES)
+def test_fused_gate_up_act_quant(mx, cases, name):
+    """gate_up with act+quant in its epilogue: bit-equal to the two stand-alone
+    launches on every row < total (codes and packed scale words, including the
+    zero padding bytes of a ragged last word), and against the oracle's codes
+    as the stand-alone act+quant is."""
+    c = cases[name]
+    g, ref = c["g"], c["ref"]
+    lay = _gpu_layout(mx, c)
+    xe, xe_s, _ = mx.expand_scatter(g["x_q"], g["x_s"], c["sl"], g["topk_w"], lay,
+                                    n_valid=g["n_valid_dev"])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    di, di_s = mx.grouped_gemm_act_quant(xe, xe_s, c["sl"], lay, g["w13"], g["s13"], status=status)
+    di_s_poison = torch.full_like(di_s, -1)
+    di2, di2_s = mx.grouped_gemm_act_quant(xe, xe_s, c["sl"], lay, g["w13"], g["s13"],
+                                           di_scale=di_s_poison, status=status)
+    gu = mx.grouped_gemm(xe, xe_s, c["sl"], lay, g["w13"], g["s13"])
+    du, du_s = mx.act_quant(gu, None, 0, c["sl"], lay.total)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    tot = ref["total"]
+    assert torch.equal(di[:tot], du[:tot])
+    assert torch.equal(di_s[:, :tot], du_s[:, :tot])
+    assert torch.equal(di2[:tot], du[:tot])
+    assert torch.equal(di2_s[:, :tot], du_s[:, :tot]), "every byte of a used scale word is written"
+    assert not di[tot:].any(), "rows past the total are untouched"
+    dg, dr = di.cpu().numpy()[:tot], ref["di"]
+    same = (dg == dr) | ((dg & 0x7F) == 0) & ((dr & 0x7F) == 0)
+    assert same.mean() >= 0.999, f"{name}: {1 - same.mean():.2e} of fp8 codes differ"
+    bg = di_s.cpu().numpy()[:, :tot].view(np.uint32)
+    assert (bg == ref["di_s"].view(np.uint32)).mean() >= 0.99
+
+
+def test_fused_gate_up_act_quant_rejects_fp32(mx, cases):
+    c = cases["mid_f32"]
+    g = c["g"]
+    lay = _gpu_layout(mx, c)
+    xe, xe_s, _ = mx.expand_scatter(g["x_q"], g["x_s"], c["sl"], g["topk_w"], lay,
+                                    n_valid=g["n_valid_dev"])
+    with pytest.raises(mx.MoEError) as ei:
+        mx.grouped_gemm_act_quant(xe, xe_s, c["sl"], lay, g["w13"], g["s13"])
+    assert ei.value.rc == -2
+
+
 @pytest.mark.parametrize("name", NAMES)
 def test_act_quant(mx, cases, name):
     c = cases[name]
