@@ -50,7 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-seconds", type=float, default=15.0)
     ap.add_argument("--unfused", action="store_true",
-                    help="ue8m0: run gate_up and act+quant as two launches")
+                    help="run gate_up and act+quant as two launches")
     ap.add_argument("--gemm-tile-n128", action="store_true",
                     help="force 128-column GEMM tiles (tuning comparison)")
     ap.add_argument("--gemm-cta-pair", action="store_true",
@@ -206,8 +206,8 @@ def run_ours(args, world, rank, local):
     gflags = (mx.MOE_GEMM_TILE_N128 if args.gemm_tile_n128 else 0) | \
         (mx.MOE_GEMM_CTA_PAIR if args.gemm_cta_pair else 0)
 
-    # ue8m0 scales: gate_up carries silu*mul and the quantiser in its epilogue
-    fused = layer.scale_mode == "ue8m0" and not args.unfused and gflags == 0
+    # gate_up carries silu*mul, the quantiser and the fold in its epilogue
+    fused = not args.unfused and gflags == 0
 
     def step(ev=None):
         def mark(i):
@@ -229,7 +229,8 @@ def run_ours(args, world, rank, local):
             mx.check(L.moe_grouped_gemm_act_quant(
                 ptr(layer.xe), ptr(layer.xe_scale), layer.sl, layer.xe_scale.shape[1],
                 ptr(lay.start), ptr(lay.tile_prefix), ptr(lay.total), ptr(layer.w13),
-                ptr(layer.s13), None, 0, cfg.E, cfg.I, cfg.H, layer.M_cap, ptr(layer.down_in),
+                ptr(layer.s13), ptr(layer.row_w), layer.flags & mx.MOE_FOLD_WEIGHT_INTO_SCALE,
+                cfg.E, cfg.I, cfg.H, layer.M_cap, ptr(layer.down_in),
                 ptr(layer.down_in_scale), layer.down_in_scale.shape[1], ptr(layer.status), s),
                 "gemm1+act_quant")
             mark(3)

@@ -161,9 +161,11 @@ def act_quant(gu: torch.Tensor, row_w: Optional[torch.Tensor], flags: int, scale
 
 def grouped_gemm_act_quant(A: torch.Tensor, A_scale: torch.Tensor, scale_layout: int, lay: Layout,
                            W13: torch.Tensor, W13_scale: torch.Tensor, flags: int = 0,
+                           row_w: Optional[torch.Tensor] = None,
                            di: Optional[torch.Tensor] = None, di_scale: Optional[torch.Tensor] = None,
                            status: Optional[torch.Tensor] = None, stream=None):
-    """gate_up GEMM with silu*mul and the fp8 quantiser fused (ue8m0 scales)."""
+    """gate_up GEMM with silu*mul and the fp8 quantiser (and, with
+    MOE_FOLD_WEIGHT_INTO_SCALE, the weight fold) in its epilogue."""
     M_cap, H = A.shape
     E, twoI, _ = W13.shape
     I = twoI // 2
@@ -173,7 +175,7 @@ def grouped_gemm_act_quant(A: torch.Tensor, A_scale: torch.Tensor, scale_layout:
         di_scale = new_scale(M_cap, I // 128, scale_layout, A.device)
     rc = load().moe_grouped_gemm_act_quant(_ptr(A), _ptr(A_scale), scale_layout, A_scale.shape[1],
                                            _ptr(lay.start), _ptr(lay.tile_prefix), _ptr(lay.total),
-                                           _ptr(W13), _ptr(W13_scale), None, flags, E, I, H, M_cap,
+                                           _ptr(W13), _ptr(W13_scale), _ptr(row_w), flags, E, I, H, M_cap,
                                            _ptr(di), _ptr(di_scale), di_scale.shape[1], _ptr(status),
                                            _stream(stream))
     check(rc, "moe_grouped_gemm_act_quant")
@@ -290,9 +292,6 @@ class ExpandedMoELayer:
                             self.H, self.K, _ptr(self.y), s), "moe_combine")
         return self.y
 
-    @property
-    def kernels_per_forward(self) -> int:
-        """Kernels one forward launches: layout 2, scatter 1, combine 1, and
-        gate_up + act+quant + down (3), or 2 where gate_up carries act+quant
-        (ue8m0 scales)."""
-        return 4 + (2 if self.scale_mode == "ue8m0" else 3)
+    # kernels one forward launches: layout 2, scatter 1, gate_up with
+    # act+quant fused 1, down 1, combine 1
+    KERNELS_PER_FORWARD = 6

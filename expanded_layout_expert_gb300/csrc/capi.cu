@@ -90,13 +90,13 @@ int moe_grouped_ffn(const uint8_t* xe, const void* xe_scale, int64_t ld_xes, int
   MOE_REQUIRE(!(flags & MOE_FOLD_WEIGHT_INTO_SCALE) || scale_layout == MOE_SCALE_F32_ROWMAJOR,
               "moe_grouped_ffn: the fold needs fp32 scales (a power-of-two scale cannot absorb a weight)");
   int rc;
-  const bool fused = scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR &&
-                     !(flags & (MOE_FFN_UNFUSED | MOE_GEMM_PER_KBLOCK_PROMOTION));
+  const bool fused = !(flags & MOE_FFN_UNFUSED);
   if (fused) {
     // gate_up with silu*mul and the quantiser in its epilogue: gateup_ws unused
-    rc = moe_grouped_gemm_act_quant(xe, xe_scale, scale_layout, ld_xes, start, tile_prefix,
-                                    d_total, w13, s13, row_w, 0, E, I, H, M_cap, down_in,
-                                    down_in_scale, ld_dis, d_status, stream);
+    rc = moe_grouped_gemm_act_quant(
+        xe, xe_scale, scale_layout, ld_xes, start, tile_prefix, d_total, w13, s13, row_w,
+        flags & (MOE_FOLD_WEIGHT_INTO_SCALE | MOE_GEMM_PER_KBLOCK_PROMOTION), E, I, H, M_cap,
+        down_in, down_in_scale, ld_dis, d_status, stream);
     if (rc != MOE_OK) return rc;
   } else {
     MOE_REQUIRE(gateup_ws, "moe_grouped_ffn: null gateup_ws");

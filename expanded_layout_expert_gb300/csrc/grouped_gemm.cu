@@ -34,6 +34,7 @@
 
 #include <atomic>
 
+#include "act_quant.cuh"
 #include "common.cuh"
 #include "gemm_host.h"
 #include "host_util.h"
@@ -54,7 +55,7 @@ constexpr int UMMA_K = 32;   // K of one tcgen05.mma for 8-bit operands
 constexpr int kMaxE = 1024;
 constexpr int kTraceWords = 8;
 
-template <int BN, bool Staged>
+template <int BN, bool Staged, bool Fused = false>
 struct Cfg {
   static constexpr int kStages = (BN == 256) ? MOE_GEMM_STAGES_256 : 6;
   static constexpr int kABytes = BM * BK;
@@ -76,15 +77,19 @@ struct Cfg {
   static constexpr int kRegsLow = 40;
   static constexpr int kRegsHigh = 232;
   static constexpr int kTmemCols = kAcc * BN;
-  static constexpr int kNumBars = 2 * kStages + 2 * kAcc + 1;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAcc + 1 + (Fused ? 4 : 0);
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem slot, abort flag
   static constexpr int kTraceOffset = kMiscOffset + 16;          // kTraceWords x u64
+  // Fused: row maxima exchanged by the two warps of a lane quarter,
+  // [2 tiles][2 halves][128 rows] fp32
+  static constexpr int kAmaxOffset = kTraceOffset + kTraceWords * 8;
+  static constexpr int kAmaxBytes = Fused ? 2 * 2 * 128 * 4 : 0;
   // Staged: per epilogue warp, 32 rows x 64 bf16 columns go through shared
   // memory for coalesced stores. It pays when tiles are short in K (the
   // store is a larger share of a tile) and costs L1 capacity otherwise (the
   // carve-out leaves less room for the cached activation-scale rows).
-  static constexpr int kStoreOffset = (kTraceOffset + kTraceWords * 8 + 1023) / 1024 * 1024;
+  static constexpr int kStoreOffset = (kAmaxOffset + kAmaxBytes + 1023) / 1024 * 1024;
   static constexpr int kStoreBytesPerWarp = Staged ? 32 * 128 : 0;
   // per-expert tables in shared memory when E <= kSmemE (else read from global)
   static constexpr int kTableOffset = kStoreOffset + kEpiWarps * kStoreBytesPerWarp;
@@ -107,6 +112,14 @@ struct Params {
   uint16_t* out;
   int32_t* status;
   unsigned long long* trace;  // optional per-CTA cycle counters
+  // Fused gate_up + act+quant: `out` holds down_proj's input codes
+  // (uint8 [M_cap, N/2]), `weight_rows` means "fold row_w into the stored
+  // scale", and these give the scales (fp32 [M_cap, ld_ds] row-major, or
+  // packed ue8m0 int32 words [ceil(N/256/4), ld_ds] written by byte). Reusing
+  // fields keeps the parameter block small: a larger one changed the
+  // register allocation of the unfused kernels and made them spill.
+  void* di_scale;
+  int64_t ld_ds;
 };
 
 // Bounded wait used while draining: no abort check, only the time limit.
@@ -134,11 +147,21 @@ enum TraceSlot {
   kTrKBlocks = 7,     // K blocks this CTA processed (count)
 };
 
-template <int BN, bool Staged>
-__global__ void __launch_bounds__(Cfg<BN, Staged>::kThreads, 1)
+// Fused (BN = 256 only): gate_up with silu(gate)*up and the fp8 quantiser of
+// down_proj's input in the epilogue (W = W13 [E, 2I, H]). A tile is 128 rows
+// x 128 intermediate columns t*128..: its B tile stacks W13's gate rows
+// [t*128, +128) over its up rows [I + t*128, +128), so each output group of
+// 128 sits in one accumulator (gate columns 0-127, up 128-255). Each
+// epilogue warp promotes gate columns [64 half, +64) with the gate block's
+// weight scale and up columns [128 + 64 half, +64) with the up block's, then
+// forms h = bf16(silu(bf16 g) * bf16 u), exchanges its row maximum with the
+// other warp of its lane quarter, and writes codes and the group's scale.
+// The arithmetic is that of the stand-alone launches, bit for bit.
+template <int BN, bool Staged, bool Fused>
+__global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using C = Cfg<BN, Staged>;
+  using C = Cfg<BN, Staged, Fused>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -147,6 +170,8 @@ __global__ void __launch_bounds__(Cfg<BN, Staged>::kThreads, 1)
   uint64_t* tfull = empty + C::kStages;
   uint64_t* tempty = tfull + C::kAcc;
   uint64_t* mma_done = tempty + C::kAcc;
+  uint64_t* amax_bar = mma_done + 1;  // Fused: [4], one per TMEM lane quarter
+  float* s_amax = reinterpret_cast<float*>(smem + C::kAmaxOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOffset + 4);
   unsigned long long* s_trace = reinterpret_cast<unsigned long long*>(smem + C::kTraceOffset);
@@ -172,6 +197,8 @@ __global__ void __launch_bounds__(Cfg<BN, Staged>::kThreads, 1)
       mbar_init(&tempty[b], C::kEpiWarps);
     }
     mbar_init(mma_done, 1);
+    if (Fused)
+      for (int q = 0; q < 4; ++q) mbar_init(&amax_bar[q], 64);  // both warps of the quarter
     *abort_flag = 0;
     for (int i = 0; i < kTraceWords; ++i) s_trace[i] = 0ull;
     fence_mbar_init();
@@ -193,7 +220,9 @@ __global__ void __launch_bounds__(Cfg<BN, Staged>::kThreads, 1)
 
   int total = *p.d_total;
   if (total > p.M_cap) total = static_cast<int>(p.M_cap);
-  const int num_n = p.N / BN;
+  // tiles per m block: BN output columns, or (fused) 128 intermediate columns
+  const int num_n = Fused ? p.N / 256 : p.N / BN;
+  const int I = p.N / 2;
   const int num_tiles = s_tp[p.E] * num_n;
   const int KB = p.Kd / BK;
   const int NB = p.N / 128;
@@ -234,7 +263,14 @@ __global__ void __launch_bounds__(Cfg<BN, Staged>::kThreads, 1)
           uint8_t* sa = smem + stage * C::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
           tma_load_2d(sa, &tmA, kb * BK, row0, &full[stage]);
-          tma_load_2d(sa + C::kABytes, &tmB, kb * BK, e * p.N + n0, &full[stage]);
+          if (Fused) {
+            const int t = tile % num_n;
+            tma_load_2d(sa + C::kABytes, &tmB, kb * BK, e * p.N + t * 128, &full[stage]);
+            tma_load_2d(sa + C::kABytes + C::kBBytes / 2, &tmB, kb * BK, e * p.N + I + t * 128,
+                        &full[stage]);
+          } else {
+            tma_load_2d(sa + C::kABytes, &tmB, kb * BK, e * p.N + n0, &full[stage]);
+          }
           ++issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
@@ -304,27 +340,35 @@ __global__ void __launch_bounds__(Cfg<BN, Staged>::kThreads, 1)
     int acc_buf = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    int iter = 0;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++iter) {
       int e, row0, rows;
       tile_rows(tile, e, row0, rows);
       const int n_tile = tile % num_n;
       const int col0 = n_tile * BN + half * C::kColsPerWarp;  // this warp's first column
-      const int nb = col0 / 128;
       const int row = row0 + row_in_tile;
       const bool row_ok = row_in_tile < rows && row < p.M_cap;
-      const int64_t wbase = (static_cast<int64_t>(e) * NB + nb) * KB;
+      // weight-scale rows of this warp's two 64-column batches: the same
+      // 128-column block, or (fused) the gate block and the up block
+      const int nb0 = Fused ? n_tile : col0 / 128;
+      const int nb1 = Fused ? I / 128 + n_tile : nb0;
+      const int64_t wbase = (static_cast<int64_t>(e) * NB + nb0) * KB;
+      const int64_t wbase1 = (static_cast<int64_t>(e) * NB + nb1) * KB;
 
       // Raw scale words, loaded two K blocks before they are used and only
       // decoded (and multiplied) then, so no load is waited for early.
       const float* asf = static_cast<const float*>(p.a_scale);
       const uint32_t* asw = static_cast<const uint32_t*>(p.a_scale);
-      auto load_raw = [&](int kb, uint32_t& ra, uint32_t& rw) {
+      auto load_raw = [&](int kb, uint32_t& ra, uint32_t& rw, uint32_t& rw1) {
         if (kb >= KB) {
           ra = 0u;
           rw = 0u;
+          rw1 = 0u;
           return;
         }
         rw = p.ue8m0 ? static_cast<uint32_t>(ws8[wbase + kb]) : __float_as_uint(wsf[wbase + kb]);
+        if (Fused)
+          rw1 = p.ue8m0 ? static_cast<uint32_t>(ws8[wbase1 + kb]) : __float_as_uint(wsf[wbase1 + kb]);
         ra = 0u;
         if (row_ok)
           ra = p.ue8m0 ? asw[static_cast<int64_t>(kb >> 2) * p.ld_as + row]
@@ -343,11 +387,11 @@ __global__ void __launch_bounds__(Cfg<BN, Staged>::kThreads, 1)
       // One K block: wait for its accumulator, read it from TMEM 16 columns
       // at a time, fold it in with the block's scale, free the buffer as
       // soon as the last read has landed.
-      auto kblock = [&](int kb, uint32_t& ra, uint32_t& rw) {
+      auto kblock = [&](int kb, uint32_t& ra, uint32_t& rw, uint32_t& rw1) {
         if (!ok || kb >= KB) return;
-        const float sc1 = decode(kb, ra, rw);
-        const float2 sc = make_float2(sc1, sc1);
-        load_raw(kb + 2, ra, rw);
+        const float sc0 = decode(kb, ra, rw);
+        const float sc1 = Fused ? decode(kb, ra, rw1) : sc0;
+        load_raw(kb + 2, ra, rw, rw1);
         // all lanes leave together: the TMEM loads below are warp-collective
         const bool got = mbar_wait(&tfull[acc_buf], acc_phase, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, got)) {
@@ -355,17 +399,20 @@ __global__ void __launch_bounds__(Cfg<BN, Staged>::kThreads, 1)
           return;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                               static_cast<uint32_t>(acc_buf * BN + half * C::kColsPerWarp);
+        const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                            static_cast<uint32_t>(acc_buf * BN);
         // 64 columns per wait; the buffer is released right after the last
         // read, before that batch is promoted, so the MMA can reuse it as
         // early as possible.
         constexpr int kBatches = C::kColsPerWarp / 64;
 #pragma unroll
         for (int bt = 0; bt < kBatches; ++bt) {
+          const uint32_t bcol = Fused ? static_cast<uint32_t>(bt * 128 + half * 64)
+                                      : static_cast<uint32_t>(half * C::kColsPerWarp + bt * 64);
+          const float2 sc = bt == 0 ? make_float2(sc0, sc0) : make_float2(sc1, sc1);
           uint32_t va[32], vb[32];
-          tc_ld32(taddr + bt * 64, va);
-          tc_ld32(taddr + bt * 64 + 32, vb);
+          tc_ld32(tq + bcol, va);
+          tc_ld32(tq + bcol + 32, vb);
           tc_wait64(va, vb);
           if (bt == kBatches - 1) {
             tc_fence_before();
@@ -389,15 +436,67 @@ __global__ void __launch_bounds__(Cfg<BN, Staged>::kThreads, 1)
         }
       };
 
-      uint32_t ra0, rw0, ra1, rw1;
-      load_raw(0, ra0, rw0);
-      load_raw(1, ra1, rw1);
+      uint32_t ra0, rw0, rx0, ra1, rw1, rx1;
+      load_raw(0, ra0, rw0, rx0);
+      load_raw(1, ra1, rw1, rx1);
       for (int kb0 = 0; kb0 < KB && ok; kb0 += 2) {
-        kblock(kb0 + 0, ra0, rw0);
-        kblock(kb0 + 1, ra1, rw1);
+        kblock(kb0 + 0, ra0, rw0, rx0);
+        kblock(kb0 + 1, ra1, rw1, rx1);
       }
       if (!ok) break;
-      if constexpr (Staged) {
+      if constexpr (Fused) {
+        // h = bf16(silu(bf16 g) * bf16 u): gate pairs acc[0..31], up acc[32..63]
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float hx = silu_mul_bf16(bf16_round(acc[j].x), bf16_round(acc[32 + j].x));
+          const float hy = silu_mul_bf16(bf16_round(acc[j].y), bf16_round(acc[32 + j].y));
+          acc[j] = make_float2(hx, hy);
+          m = fmaxf(m, fmaxf(fabsf(hx), fabsf(hy)));
+        }
+        // the other warp's maximum for the same row (double-buffered by tile)
+        const int par = iter & 1;
+        s_amax[(par * 2 + half) * 128 + row_in_tile] = m;
+        mbar_arrive(&amax_bar[quarter]);
+        const bool got = mbar_wait(&amax_bar[quarter], static_cast<uint32_t>(par), abort_flag,
+                                   p.status);
+        if (!__all_sync(0xffffffffu, got)) break;
+        const float amax = fmaxf(m, s_amax[(par * 2 + (half ^ 1)) * 128 + row_in_tile]);
+        float sc, inv;
+        uint32_t bexp;
+        group_scale(amax, p.ue8m0 != 0, sc, inv, bexp);
+        if (row_ok) {
+          uint8_t* di = reinterpret_cast<uint8_t*>(p.out);
+          uint4* dst = reinterpret_cast<uint4*>(di + static_cast<int64_t>(row) * I +
+                                                n_tile * 128 + half * 64);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float h[16] = {acc[8 * q + 0].x, acc[8 * q + 0].y, acc[8 * q + 1].x,
+                                 acc[8 * q + 1].y, acc[8 * q + 2].x, acc[8 * q + 2].y,
+                                 acc[8 * q + 3].x, acc[8 * q + 3].y, acc[8 * q + 4].x,
+                                 acc[8 * q + 4].y, acc[8 * q + 5].x, acc[8 * q + 5].y,
+                                 acc[8 * q + 6].x, acc[8 * q + 6].y, acc[8 * q + 7].x,
+                                 acc[8 * q + 7].y};
+            const uint2 lo = fp8x8(h, inv), hi = fp8x8(h + 8, inv);
+            dst[q] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          }
+          if (half == 0) {
+            if (p.ue8m0) {
+              // byte t%4 of word (t/4, row); the last group also clears the
+              // word's unused bytes
+              uint8_t* w = static_cast<uint8_t*>(p.di_scale) +
+                           (static_cast<int64_t>(n_tile >> 2) * p.ld_ds + row) * 4;
+              w[n_tile & 3] = static_cast<uint8_t>(bexp);
+              if (n_tile == num_n - 1)
+                for (int z = (n_tile & 3) + 1; z < 4; ++z) w[z] = 0;
+            } else {
+              const float wgt = p.weight_rows ? p.row_w[row] : 1.0f;
+              static_cast<float*>(p.di_scale)[static_cast<int64_t>(row) * p.ld_ds + n_tile] =
+                  __fmul_rn(sc, wgt);
+            }
+          }
+        }
+      } else if constexpr (Staged) {
       // Store through shared memory: each thread writes its row's 64-column
       // slices (swizzled, conflict-free), then the warp writes 4 rows of 128
       // contiguous bytes per instruction.
@@ -806,19 +905,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
 
 std::atomic<unsigned long long*> g_trace{nullptr};
 
-template <int BN, bool Staged>
+template <int BN, bool Staged, bool Fused = false>
 int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm, cudaStream_t s) {
-  using C = Cfg<BN, Staged>;
+  using C = Cfg<BN, Staged, Fused>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<BN, Staged>,
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<BN, Staged, Fused>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
       return check_launch("cudaFuncSetAttribute(grouped_gemm_kernel)");
     attr_set[dev] = true;
   }
-  grouped_gemm_kernel<BN, Staged><<<device_sm_count(), C::kThreads, C::kSmemBytes, s>>>(ta, tb, prm);
+  grouped_gemm_kernel<BN, Staged, Fused><<<device_sm_count(), C::kThreads, C::kSmemBytes, s>>>(
+      ta, tb, prm);
   return check_launch("grouped_gemm_kernel");
 }
 
@@ -918,6 +1018,8 @@ extern "C" int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale
   prm.out = out;
   prm.status = d_status;
   prm.trace = moe::g_trace.load();
+  prm.di_scale = nullptr;
+  prm.ld_ds = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (pair) return moe::launch_pair(ta, tb, prm, s);
   // Short-K GEMMs (down_proj) spend a larger share of each tile on the
@@ -942,19 +1044,52 @@ extern "C" int moe_grouped_gemm_act_quant(const uint8_t* A, const void* A_scale,
               "moe_grouped_gemm_act_quant: I and H must be positive multiples of 128");
   MOE_REQUIRE(M_cap > 0 && M_cap <= INT32_MAX && static_cast<int64_t>(E) * 2 * I <= INT32_MAX,
               "moe_grouped_gemm_act_quant: sizes exceed int32");
-  if (scale_layout != MOE_SCALE_UE8M0_PACKED_COLMAJOR) {
-    moe::set_error("moe_grouped_gemm_act_quant: the fused path takes ue8m0 scales");
-    return MOE_ERR_UNSUPPORTED;
+  MOE_REQUIRE(scale_layout == MOE_SCALE_F32_ROWMAJOR || scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR,
+              "moe_grouped_gemm_act_quant: bad scale layout");
+  const bool ue8m0 = scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR;
+  const bool fold = (flags & MOE_FOLD_WEIGHT_INTO_SCALE) != 0;
+  MOE_REQUIRE(!fold || (!ue8m0 && row_w),
+              "moe_grouped_gemm_act_quant: the fold needs row_w and fp32 scales");
+  if (ue8m0) {
+    MOE_REQUIRE(ld_as >= M_cap && ld_ds >= M_cap,
+                "moe_grouped_gemm_act_quant: packed scale leading dimension < M_cap");
+  } else {
+    MOE_REQUIRE(ld_as >= H / 128 && ld_ds >= I / 128,
+                "moe_grouped_gemm_act_quant: scale leading dimension too small");
   }
-  MOE_REQUIRE(!(flags & MOE_FOLD_WEIGHT_INTO_SCALE),
-              "moe_grouped_gemm_act_quant: a power-of-two scale cannot absorb the weight");
-  MOE_REQUIRE(ld_as >= M_cap && ld_ds >= M_cap,
-              "moe_grouped_gemm_act_quant: packed scale leading dimension < M_cap");
   MOE_REQUIRE(moe::aligned(A, 16) && moe::aligned(W13, 16) && moe::aligned(di, 16) &&
                   moe::aligned(di_scale, 4),
               "moe_grouped_gemm_act_quant: A, W13 and di must be 16-byte aligned");
   MOE_REQUIRE_DEVICE();
-  (void)row_w;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!ue8m0 || (flags & MOE_GEMM_PER_KBLOCK_PROMOTION)) {
+    // fp32 scales: per-K-block promotion kernel with the fused epilogue
+    CUtensorMap ta, tb;
+    int rc = moe::make_tmap_k128(&ta, A, H, M_cap, H, moe::BM);
+    if (rc != MOE_OK) return rc;
+    rc = moe::make_tmap_k128(&tb, W13, H, static_cast<uint64_t>(E) * 2 * I, H, 128);
+    if (rc != MOE_OK) return rc;
+    moe::Params prm;
+    prm.a_scale = A_scale;
+    prm.ld_as = ld_as;
+    prm.ue8m0 = ue8m0 ? 1 : 0;
+    prm.w_scale = W13_scale;
+    prm.start = start;
+    prm.tile_prefix = tile_prefix;
+    prm.d_total = d_total;
+    prm.row_w = row_w;
+    prm.weight_rows = fold ? 1 : 0;  // fused: fold the weight into the stored scale
+    prm.E = E;
+    prm.N = 2 * I;
+    prm.Kd = H;
+    prm.M_cap = M_cap;
+    prm.out = reinterpret_cast<uint16_t*>(di);  // fused: the fp8 codes
+    prm.status = d_status;
+    prm.trace = moe::g_trace.load();
+    prm.di_scale = di_scale;
+    prm.ld_ds = ld_ds;
+    return moe::launch<256, false, true>(ta, tb, prm, s);
+  }
   moe::MxGemmArgs a;
   a.A = A;
   a.A_scale = static_cast<const uint32_t*>(A_scale);
@@ -975,5 +1110,5 @@ extern "C" int moe_grouped_gemm_act_quant(const uint8_t* A, const void* A_scale,
   a.di = di;
   a.di_scale = static_cast<uint8_t*>(di_scale);
   a.ld_ds = ld_ds;
-  return moe::launch_grouped_gemm_mx(a, reinterpret_cast<cudaStream_t>(stream));
+  return moe::launch_grouped_gemm_mx(a, s);
 }

@@ -214,10 +214,13 @@ int moe_act_quant(const uint16_t* gu, int I, const float* row_w, int flags, int 
  *   W13      device uint8 [E, 2I, H]: gate rows [0, I), up rows [I, 2I)
  *   di       device uint8 [M_cap, I], 16-byte aligned; rows r < *d_total written
  *   di_scale packed ue8m0 int32 [ceil(I/512), ld_ds], ld_ds >= M_cap
- * Takes scale_layout MOE_SCALE_UE8M0_PACKED_COLMAJOR (the tensor core applies
- * the power-of-two scales); returns MOE_ERR_UNSUPPORTED for fp32 scales, whose
- * callers use the two-launch path. row_w is unused (a power-of-two scale
- * cannot absorb the weight; weight down_proj's output rows instead).
+ *   row_w    device fp32 [M_cap], read with MOE_FOLD_WEIGHT_INTO_SCALE (fp32
+ *            scales only: the stored scale is s * row_w[r], as moe_act_quant)
+ *   flags    MOE_FOLD_WEIGHT_INTO_SCALE, MOE_GEMM_PER_KBLOCK_PROMOTION
+ * Both scale layouts: ue8m0 scales go to the tensor core's block scaling,
+ * fp32 scales to the per-K-block promotion kernel; either way the epilogue
+ * forms h = bf16(silu(g) u) per 128-column group and writes its codes and
+ * scale. Needs I % 128 == 0, H % 128 == 0, E <= 1024.
  */
 int moe_grouped_gemm_act_quant(const uint8_t* A, const void* A_scale, int scale_layout,
                                int64_t ld_as, const int32_t* start, const int32_t* tile_prefix,
@@ -234,9 +237,9 @@ int moe_grouped_gemm_act_quant(const uint8_t* A, const void* A_scale, int scale_
  * flags: MOE_FOLD_WEIGHT_INTO_SCALE (fp32 scales) or MOE_WEIGHT_OUTPUT_ROWS
  * (ue8m0 scales; a power-of-two scale cannot absorb the weight, so the output
  * row is weighted instead), or 0 (unweighted; moe_combine may weight).
- * With ue8m0 scales the first two steps run as one launch
- * (moe_grouped_gemm_act_quant) and gateup_ws is not touched (it may be NULL);
- * MOE_FFN_UNFUSED or MOE_GEMM_PER_KBLOCK_PROMOTION keep three launches.
+ * The first two steps run as one launch (moe_grouped_gemm_act_quant) and
+ * gateup_ws is not touched (it may be NULL); MOE_FFN_UNFUSED keeps three
+ * launches (gateup_ws required).
  */
 int moe_grouped_ffn(const uint8_t* xe, const void* xe_scale, int64_t ld_xes, int scale_layout,
                     const int32_t* start, const int32_t* tile_prefix, const int32_t* d_total,

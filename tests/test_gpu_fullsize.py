@@ -5,8 +5,8 @@ configuration the benchmark times):
   cheap at any size);
 * scatter: every expanded row equals its token's bytes, scale and weight, and
   every alignment gap is zero (a property checked on all rows on the device);
-* ue8m0: the fused gate_up + act+quant equals the stand-alone launches on
-  every row, bit for bit;
+* the fused gate_up + act+quant of the forward equals the stand-alone
+  launches on every row, bit for bit;
 * gate_up rows and final outputs on sampled tokens against the oracle, which
   computes them one by one (the final output to rel-Frobenius <= 1e-2 and
   max abs <= 5e-2);
@@ -82,15 +82,19 @@ def test_workload_full_size(mx, orc, cfg):
     gap[rows] = False
     assert not layer.xe[:total][gap].any() and not layer.row_w[:total][gap].any()
 
+    # the forward ran gate_up with act+quant fused; the two stand-alone
+    # launches give the same codes and scales on every row
+    gu = mx.grouped_gemm(layer.xe, layer.xe_scale, layer.sl, lay, layer.w13, layer.s13,
+                         out=layer.gateup)
+    fold = layer.flags & mx.MOE_FOLD_WEIGHT_INTO_SCALE
+    du, du_s = mx.act_quant(gu, layer.row_w, fold, layer.sl, lay.total)
+    torch.cuda.synchronize()
+    assert torch.equal(du[:total], layer.down_in[:total])
     if cfg.scale_mode == "ue8m0":
-        # the forward ran gate_up with act+quant fused; the two stand-alone
-        # launches give the same codes and scale words on every row
-        gu = mx.grouped_gemm(layer.xe, layer.xe_scale, layer.sl, lay, layer.w13, layer.s13,
-                             out=layer.gateup)
-        du, du_s = mx.act_quant(gu, None, 0, layer.sl, lay.total)
-        torch.cuda.synchronize()
-        assert torch.equal(du[:total], layer.down_in[:total])
         assert torch.equal(du_s[:, :total], layer.down_in_scale[:, :total])
+    else:
+        assert torch.equal(du_s[:total].view(torch.int32),
+                           layer.down_in_scale[:total].view(torch.int32))
 
     # rows past n_valid untouched
     if nv < cfg.T:
