@@ -141,8 +141,8 @@ enum TraceSlot {
   kTrProdWait = 1,    // producer waiting for a free stage
   kTrMmaWaitTmem = 2, // MMA waiting for a free TMEM buffer
   kTrMmaWaitData = 3, // MMA waiting for TMA data
-  kTrUnused4 = 4,
-  kTrUnused5 = 5,
+  kTrEpiWait = 4,     // epilogue warp 4: waiting for a full accumulator
+  kTrEpiTile = 5,     // epilogue warp 4: tile-end work (store, or act+quant)
   kTrUnused6 = 6,
   kTrKBlocks = 7,     // K blocks this CTA processed (count)
 };
@@ -341,6 +341,7 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     int iter = 0;
+    unsigned long long t_epi_wait = 0, t_epi_tile = 0;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++iter) {
       int e, row0, rows;
       tile_rows(tile, e, row0, rows);
@@ -393,7 +394,9 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
         const float sc1 = Fused ? decode(kb, ra, rw1) : sc0;
         load_raw(kb + 2, ra, rw, rw1);
         // all lanes leave together: the TMEM loads below are warp-collective
+        const long long tw0 = tracing ? clock64() : 0;
         const bool got = mbar_wait(&tfull[acc_buf], acc_phase, abort_flag, p.status);
+        if (tracing) t_epi_wait += clock64() - tw0;
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           return;
@@ -444,6 +447,7 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
         kblock(kb0 + 1, ra1, rw1, rx1);
       }
       if (!ok) break;
+      const long long tt0 = tracing ? clock64() : 0;
       if constexpr (Fused) {
         // h = bf16(silu(bf16 g) * bf16 u): gate pairs acc[0..31], up acc[32..63]
         float m = 0.0f;
@@ -554,6 +558,11 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
           }
         }
       }
+      if (tracing) t_epi_tile += clock64() - tt0;
+    }
+    if (tracing && ew == 0 && lane == 0) {
+      s_trace[kTrEpiWait] = t_epi_wait;
+      s_trace[kTrEpiTile] = t_epi_tile;
     }
   }
 
