@@ -37,6 +37,16 @@ WORKLOAD = synth.CONFIGS[2]          # zipf_t16384_h7168
 L2_FLUSH_BYTES = 256 << 20           # > the 126 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_PER_BF16 = 2.0                   # nominal dense fp8 : bf16 tensor rate
+# DRAM bytes (read + write) of one launch of the dominant kernel (gate_up with
+# act+quant in its epilogue) on the full workload, from one ncu capture of
+# this build:  python bench.py --workload W --steps 1 --warmup 3
+# --no-cpu-baseline --no-e2e, under ncu --metrics
+# dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
+# -k regex:grouped_gemm -s 6 -c 1. Update it whenever that kernel changes.
+GATE_UP_DRAM_BYTES = {
+    "zipf_t16384_h7168": 1805949952 + 262330112,
+    "ue8m0_t8192_h7168": 2857351936 + 142681088,
+}
 
 
 def parse_args(argv=None):
@@ -337,7 +347,8 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "tensor",
                      "kernel": "grouped_gemm (gate_up" + (" + act_quant epilogue)" if fused else ")"),
                      "achieved": kernels["gemm1"]["achieved"], "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": kernels["gemm1"]["frac"], "traffic": None,
+                     "unit": "TFLOP/s", "frac": kernels["gemm1"]["frac"],
+                     "traffic": GATE_UP_DRAM_BYTES.get(cfg.name) if fused else None,
                      "peak_source": f"{peak_src}: bf16 burst x {FP8_PER_BF16:g} (nominal fp8:bf16)"},
         "gpu_launches": (6 if fused else 7) * args.steps,
         "clocks": clocks.summary(),
