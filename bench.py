@@ -59,6 +59,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-seconds", type=float, default=15.0)
+    ap.add_argument("--weighting", choices=["expanded", "gather"], default="expanded",
+                    help="expanded: fold / output-row weighting (do_expand=True); gather: "
+                         "weights applied in the combine (the do_expand=False A/B arrangement)")
     ap.add_argument("--unfused", action="store_true",
                     help="run gate_up and act+quant as two launches")
     ap.add_argument("--gemm-tile-n128", action="store_true",
@@ -204,7 +207,7 @@ def run_ours(args, world, rank, local):
     nv = d["n_valid"]
     n_valid = torch.tensor([nv], dtype=torch.int32, device=dev)
     layer = mx.ExpandedMoELayer(d["w13"], d["s13"], d["w2"], d["s2"], K=cfg.K, align=cfg.align,
-                                scale_mode=cfg.scale_mode, max_tokens=cfg.T)
+                                scale_mode=cfg.scale_mode, max_tokens=cfg.T, weighting=args.weighting)
     L = mx.load()
     stream = torch.cuda.current_stream()
     s = stream.cuda_stream
@@ -265,7 +268,8 @@ def run_ours(args, world, rank, local):
                                     (layer.flags & mx.MOE_WEIGHT_OUTPUT_ROWS) | gflags, cfg.E, cfg.H, cfg.I,
                                     layer.M_cap, ptr(layer.down_out), ptr(layer.status), s), "gemm2")
         mark(5)
-        mx.check(L.moe_combine(ptr(layer.down_out), ptr(lay.src2dst), None, ptr(n_valid), cfg.T,
+        gather_w = layer.row_w if layer.weighting == "gather" else None
+        mx.check(L.moe_combine(ptr(layer.down_out), ptr(lay.src2dst), ptr(gather_w), ptr(n_valid), cfg.T,
                                cfg.H, cfg.K, ptr(layer.y), s), "combine")
         mark(6)
 
@@ -338,6 +342,7 @@ def run_ours(args, world, rank, local):
                    "routing": (f"zipf(s={cfg.zipf_s}), {cfg.zipf_zero_experts} experts empty"
                                if cfg.routing == "zipf" else cfg.routing),
                    "inactive_rows": cfg.inactive_frac, "scales": cfg.scale_mode,
+                   "weighting": args.weighting,
                    "valid_pairs": P, "expanded_rows": M_pad, "M_cap": layer.M_cap,
                    "l2": "flushed between steps (256 MiB write outside the timed events)",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},

@@ -227,19 +227,28 @@ class ExpandedMoELayer:
                packed ue8m0 exponents (scale_mode "ue8m0")
       topk_ids int32 [T, K], -1 = no pair; topk_w fp32 [T, K]
       n_valid  optional int32 [1] device tensor: rows >= n_valid are padding
-    On the fp32 path the top-k weight is folded into down_proj's input
-    scale; on the ue8m0 path it multiplies the down_proj output rows.
+    weighting "expanded" (default): on the fp32 path the top-k weight is
+    folded into down_proj's input scale; on the ue8m0 path it multiplies the
+    down_proj output rows; the combine sums unweighted.
+    weighting "gather": the do_expand=False arrangement (ep_gather): no fold,
+    the combine multiplies each pair's row by its weight while summing.
     """
 
     def __init__(self, w13, s13, w2, s2, *, K: int, align: int, scale_mode: str,
-                 max_tokens: int, device=None):
+                 max_tokens: int, device=None, weighting: str = "expanded"):
         self.w13, self.s13, self.w2, self.s2 = w13, s13, w2, s2
         self.E, twoI, self.H = w13.shape
         self.I = twoI // 2
         self.K, self.align = K, align
         self.scale_mode = scale_mode
         self.sl = scale_layout_of(scale_mode)
-        self.flags = MOE_WEIGHT_OUTPUT_ROWS if scale_mode == "ue8m0" else MOE_FOLD_WEIGHT_INTO_SCALE
+        if weighting not in ("expanded", "gather"):
+            raise ValueError(f"weighting must be 'expanded' or 'gather', got {weighting!r}")
+        self.weighting = weighting
+        if weighting == "gather":
+            self.flags = 0
+        else:
+            self.flags = MOE_WEIGHT_OUTPUT_ROWS if scale_mode == "ue8m0" else MOE_FOLD_WEIGHT_INTO_SCALE
         self.T = max_tokens
         dev = device if device is not None else w13.device
         self.device = dev
@@ -288,8 +297,9 @@ class ExpandedMoELayer:
                                 _ptr(self.gateup), _ptr(self.down_in), _ptr(self.down_in_scale),
                                 self.down_in_scale.shape[1], _ptr(self.down_out),
                                 _ptr(self.status), s), "moe_grouped_ffn")
-        check(L.moe_combine(_ptr(self.down_out), _ptr(lay.src2dst), None, _ptr(n_valid), T,
-                            self.H, self.K, _ptr(self.y), s), "moe_combine")
+        gather_w = self.row_w if self.weighting == "gather" else None
+        check(L.moe_combine(_ptr(self.down_out), _ptr(lay.src2dst), _ptr(gather_w), _ptr(n_valid),
+                            T, self.H, self.K, _ptr(self.y), s), "moe_combine")
         return self.y
 
     # kernels one forward launches: layout 2, scatter 1, gate_up with

@@ -276,10 +276,20 @@ def to_numpy_inputs(d: dict) -> dict:
     return out
 
 
-def run_layer(inp: dict, M_cap: int) -> dict:
+def run_layer(inp: dict, M_cap: int, weighting: str = "expanded") -> dict:
     """The whole expanded layer, every row, in the layer's order: layout,
     scatter, gate_up GEMM, activation + quant (+ fold), down GEMM, (ue8m0:
-    output-row weighting), combine. Returns every intermediate."""
+    output-row weighting), combine. Returns every intermediate.
+
+    weighting "expanded": the top-k weight is folded into down_proj's fp32
+    input scale, or on the ue8m0 path multiplies the down_proj output rows
+    (SGLang PR 37261, Modifications/Core), and the combine sums unweighted.
+    weighting "gather": the do_expand=False arrangement of the same PR's A/B
+    baseline, where ep_gather applies the weights while summing
+    (post_permute_deep_gemm_to_deepep_v2's non-expanded branch): no fold, no
+    row weighting, y[t] = bf16(sum_k w[t,k] * down[row(t,k)])."""
+    if weighting not in ("expanded", "gather"):
+        raise ValueError(weighting)
     cfg = inp["cfg"]
     sl = inp["scale_layout"]
     nv = inp["n_valid"]
@@ -293,13 +303,18 @@ def run_layer(inp: dict, M_cap: int) -> dict:
     experts = lay["m_indices"][:total]
     ld_xes = xe_s.shape[1]
     gu = gemm_rows(xe, xe_s, sl, ld_xes, rows, experts, inp["w13"], inp["s13"])
-    if sl == SCALE_F32:
-        di, di_s = act_quant_rows(gu, row_w[:total], sl)
-        down = gemm_rows(di, di_s, sl, di_s.shape[1], rows, experts, inp["w2"], inp["s2"])
-    else:
+    if weighting == "gather":
         di, di_s = act_quant_rows(gu, None, sl)
-        down_u = gemm_rows(di, di_s, sl, di_s.shape[1], rows, experts, inp["w2"], inp["s2"])
-        down = weight_rows(down_u, row_w[:total])
-    y = combine(down, lay["src2dst"], None, nv, T)
+        down = gemm_rows(di, di_s, sl, di_s.shape[1], rows, experts, inp["w2"], inp["s2"])
+        y = combine(down, lay["src2dst"], row_w, nv, T)
+    else:
+        if sl == SCALE_F32:
+            di, di_s = act_quant_rows(gu, row_w[:total], sl)
+            down = gemm_rows(di, di_s, sl, di_s.shape[1], rows, experts, inp["w2"], inp["s2"])
+        else:
+            di, di_s = act_quant_rows(gu, None, sl)
+            down_u = gemm_rows(di, di_s, sl, di_s.shape[1], rows, experts, inp["w2"], inp["s2"])
+            down = weight_rows(down_u, row_w[:total])
+        y = combine(down, lay["src2dst"], None, nv, T)
     return dict(layout=lay, xe=xe, xe_s=xe_s, row_w=row_w, gu=gu, di=di, di_s=di_s,
                 down=down, y=y, total=total)

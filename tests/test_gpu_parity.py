@@ -234,10 +234,43 @@ def test_combine(mx, cases, name):
     assert torch.isnan(y[nv:].float()).all(), "rows past n_valid must not be written"
 
 
-def _layer(mx, c):
+@pytest.mark.parametrize("name", NAMES)
+def test_weighted_combine(mx, cases, orc, name):
+    """The gather-weighted combine (ep_gather's weighting) against the oracle's
+    weighted sum on the oracle's unweighted down rows."""
+    c = cases[name]
+    cfg, g, ref, M = c["cfg"], c["g"], c["ref"], c["M_cap"]
+    gref = c.setdefault("gather_ref", orc.run_layer(c["inp"], M, weighting="gather"))
+    lay = _gpu_layout(mx, c)
+    down = torch.from_numpy(_pad_rows(gref["down"], M).view(np.int16)).view(torch.bfloat16).cuda()
+    row_w = torch.from_numpy(_pad_rows(gref["row_w"], M)).cuda()
+    y = torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mx.combine(down, lay.src2dst, row_w, g["n_valid_dev"], y)
+    torch.cuda.synchronize()
+    nv = c["inp"]["n_valid"]
+    assert_bf16_close(u16(y)[:nv], gref["y"][:nv], f"{name} weighted combine")
+    assert torch.isnan(y[nv:].float()).all(), "rows past n_valid must not be written"
+
+
+def _layer(mx, c, weighting="expanded"):
     cfg, g = c["cfg"], c["g"]
     return mx.ExpandedMoELayer(g["w13"], g["s13"], g["w2"], g["s2"], K=cfg.K, align=cfg.align,
-                               scale_mode=cfg.scale_mode, max_tokens=cfg.T)
+                               scale_mode=cfg.scale_mode, max_tokens=cfg.T, weighting=weighting)
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_layer_gather_weighting_end_to_end(mx, cases, orc, name):
+    """The do_expand=False arrangement (weights applied in the combine) against
+    the oracle's layer with the same arrangement."""
+    c = cases[name]
+    g = c["g"]
+    gref = c.setdefault("gather_ref", orc.run_layer(c["inp"], c["M_cap"], weighting="gather"))
+    layer = _layer(mx, c, weighting="gather")
+    y = layer.forward(g["x_q"], g["x_s"], g["topk_ids"], g["topk_w"], g["n_valid_dev"])
+    torch.cuda.synchronize()
+    assert layer.status.item() == 0
+    nv = c["inp"]["n_valid"]
+    assert_final_close(u16(y)[:nv], gref["y"][:nv], name)
 
 
 @pytest.mark.parametrize("name", NAMES)

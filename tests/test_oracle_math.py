@@ -214,3 +214,62 @@ def test_poisoned_tail_changes_nothing(orc, layer_runs):
     assert np.array_equal(out2["y"][:nv], out["y"][:nv])
     for key in ("xe", "gu", "di", "down"):
         assert np.array_equal(out2[key], out[key])
+
+
+def test_gather_weighting_differs_from_the_fold_only_in_the_stored_scale(orc, layer_runs):
+    """The do_expand=False arrangement (weights applied while gathering) runs
+    the same GEMMs on the same codes: gate_up is identical, the fp8 codes are
+    identical, and the fold's stored scale is exactly fl(s * w)."""
+    inp, out, M_cap = layer_runs["mid_f32"]
+    g = orc.run_layer(inp, M_cap, weighting="gather")
+    tot = out["total"]
+    assert np.array_equal(g["gu"], out["gu"])
+    assert np.array_equal(g["di"], out["di"])
+    w = out["row_w"][:tot].astype(np.float32)
+    folded = (g["di_s"].astype(np.float32) * w[:, None]).astype(np.float32)
+    assert np.array_equal(folded.view(np.uint32), out["di_s"].view(np.uint32))
+    nv = inp["n_valid"]
+    a = orc.bf16_decode(g["y"][:nv])
+    b = orc.bf16_decode(out["y"][:nv])
+    assert np.linalg.norm(a - b) <= 1e-2 * np.linalg.norm(b)
+
+
+def test_weighted_combine_invariants(orc, layer_runs):
+    """Unit weights give the unweighted sum bit for bit; weights of 2 (exact
+    in every format) give twice it bit for bit; a -1 pair adds nothing."""
+    inp, out, _ = layer_runs["mid_zipf_ragged"]
+    nv, T = inp["n_valid"], inp["topk_ids"].shape[0]
+    s2d = out["layout"]["src2dst"]
+    down = out["down"]
+    ones = np.ones(out["row_w"].shape, np.float32)
+    y0 = orc.combine(down, s2d, None, nv, T)
+    assert np.array_equal(orc.combine(down, s2d, ones, nv, T), y0)
+    y2 = orc.combine(down, s2d, 2 * ones, nv, T)
+    assert np.array_equal(orc.bf16_decode(y2), 2 * orc.bf16_decode(y0))
+    assert np.array_equal(y0, out["y"])
+
+
+def test_gather_layer_equals_sum_of_weighted_single_pair_paths(orc, layer_runs):
+    """Gather weighting on tiny inputs, against the definition pair by pair:
+    y[t] = bf16(sum_k w[t,k] * f(x_t, e_k)), f the unweighted expert FFN taken
+    as the layer output of that one pair with weight 1."""
+    inp, out, M_cap = layer_runs["tiny_h512"]
+    g = orc.run_layer(inp, M_cap, weighting="gather")
+    ids, w = inp["topk_ids"], inp["topk_w"]
+    for t in range(0, 12):
+        if (ids[t] < 0).all():
+            assert (g["y"][t] == 0).all()
+            continue
+        acc = np.zeros(inp["x_q"].shape[1])
+        for k in range(ids.shape[1]):
+            if ids[t, k] < 0:
+                continue
+            one = dict(inp)
+            only = -np.ones_like(ids)
+            only[t, k] = ids[t, k]
+            one["topk_ids"] = only
+            unit = inp["topk_w"].copy()
+            unit[t, k] = 1.0
+            one["topk_w"] = unit
+            acc += float(w[t, k]) * orc.bf16_decode(orc.token_forward(one, t))
+        assert np.array_equal(orc.bf16_encode(acc), g["y"][t]), t
