@@ -22,7 +22,8 @@ from ._capi import (MOE_BLOCK_M, MOE_FFN_UNFUSED, MOE_FOLD_WEIGHT_INTO_SCALE, MO
 
 __all__ = [
     "expanded_capacity", "workspace_size", "expand_layout", "expand_scatter", "grouped_gemm",
-    "act_quant", "grouped_gemm_act_quant", "grouped_ffn", "combine", "ExpandedMoELayer", "Layout",
+    "act_quant", "grouped_gemm_act_quant", "grouped_ffn", "combine", "ExpandedMoELayer",
+    "HostPipeline", "Layout",
     "MoEError",
     "MOE_SCALE_F32_ROWMAJOR", "MOE_SCALE_UE8M0_PACKED_COLMAJOR", "MOE_FOLD_WEIGHT_INTO_SCALE",
     "MOE_WEIGHT_OUTPUT_ROWS", "MOE_GEMM_TILE_N128", "MOE_GEMM_CTA_PAIR",
@@ -266,14 +267,19 @@ class ExpandedMoELayer:
         self.xe = torch.zeros(M, H, dtype=torch.uint8, device=dev)
         self.xe_scale = new_scale(M, H // 128, self.sl, dev)
         self.row_w = torch.zeros(M, dtype=torch.float32, device=dev)
-        self.gateup = torch.zeros(M, 2 * I, dtype=torch.bfloat16, device=dev)
+        self._gateup = None  # bf16 [M_cap, 2I], only for the stand-alone gate_up
         self.down_in = torch.zeros(M, I, dtype=torch.uint8, device=dev)
         self.down_in_scale = new_scale(M, I // 128, self.sl, dev)
         self.down_out = torch.zeros(M, H, dtype=torch.bfloat16, device=dev)
         self.y = torch.zeros(max_tokens, H, dtype=torch.bfloat16, device=dev)
 
-    def forward(self, x_q, x_scale, topk_ids, topk_w, n_valid=None, stream=None) -> torch.Tensor:
+    def forward(self, x_q, x_scale, topk_ids, topk_w, n_valid=None, stream=None,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """y (self.y, or ``out``: bf16 [T, H]; rows >= n_valid not written)."""
         T = x_q.shape[0]
+        y = self.y if out is None else out
+        if y.shape != (self.T, self.H) or y.dtype != torch.bfloat16 or not y.is_contiguous():
+            raise ValueError("out must be a contiguous bf16 [T, H] tensor")
         if T != self.T:
             raise ValueError(f"layer was built for {self.T} token rows, got {T}")
         L = load()
@@ -294,14 +300,94 @@ class ExpandedMoELayer:
                                 self.sl, _ptr(lay.start), _ptr(lay.tile_prefix), _ptr(lay.total),
                                 _ptr(self.w13), _ptr(self.s13), _ptr(self.w2), _ptr(self.s2),
                                 _ptr(self.row_w), self.flags, self.E, self.H, self.I, self.M_cap,
-                                _ptr(self.gateup), _ptr(self.down_in), _ptr(self.down_in_scale),
+                                None, _ptr(self.down_in), _ptr(self.down_in_scale),
                                 self.down_in_scale.shape[1], _ptr(self.down_out),
                                 _ptr(self.status), s), "moe_grouped_ffn")
         gather_w = self.row_w if self.weighting == "gather" else None
         check(L.moe_combine(_ptr(self.down_out), _ptr(lay.src2dst), _ptr(gather_w), _ptr(n_valid),
-                            T, self.H, self.K, _ptr(self.y), s), "moe_combine")
-        return self.y
+                            T, self.H, self.K, _ptr(y), s), "moe_combine")
+        return y
+
+    @property
+    def gateup(self) -> torch.Tensor:
+        """bf16 [M_cap, 2I] buffer for the stand-alone gate_up GEMM (the
+        layer's own forward fuses act+quant into gate_up and never needs it)."""
+        if self._gateup is None:
+            self._gateup = torch.zeros(self.M_cap, 2 * self.I, dtype=torch.bfloat16,
+                                       device=self.device)
+        return self._gateup
 
     # kernels one forward launches: layout 2, scatter 1, gate_up with
     # act+quant fused 1, down 1, combine 1
     KERNELS_PER_FORWARD = 6
+
+
+class HostPipeline:
+    """Runs an ExpandedMoELayer on batches held in pinned host memory with the
+    copies off the critical path: batch k+1's inputs go host->device on one
+    copy stream and batch k's output device->host on another while the
+    layer's kernels run batch k on the compute stream. Device inputs and
+    outputs are double-buffered; every batch's copies still happen.
+
+        pipe = HostPipeline(layer)
+        for batch, y_host in ...:
+            pipe.submit(x_q_h, x_s_h, ids_h, w_h, n_valid_h, y_host)
+        pipe.synchronize()        # every y_host filled
+
+    Host tensors must be pinned (page-locked) for the copies to be
+    asynchronous, and a y_host may be read only after synchronize() (or after
+    the submit two batches later has returned and its event completed).
+    """
+
+    def __init__(self, layer: "ExpandedMoELayer", stream=None):
+        self.layer = layer
+        dev = layer.device
+        self.comp = stream if stream is not None else torch.cuda.current_stream(dev)
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        T, H, K = layer.T, layer.H, layer.K
+        G = H // 128
+        def bufs():
+            xs = (torch.empty(T, G, dtype=torch.float32, device=dev) if layer.sl == 0 else
+                  torch.empty((G + 3) // 4, T, dtype=torch.int32, device=dev))
+            return dict(x_q=torch.empty(T, H, dtype=torch.uint8, device=dev), x_s=xs,
+                        ids=torch.empty(T, K, dtype=torch.int32, device=dev),
+                        w=torch.empty(T, K, dtype=torch.float32, device=dev),
+                        nv=torch.empty(1, dtype=torch.int32, device=dev),
+                        y=torch.zeros(T, H, dtype=torch.bfloat16, device=dev))
+        self.bufs = [bufs(), bufs()]
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.done = [torch.cuda.Event() for _ in range(2)]
+        self.out_copied = [torch.cuda.Event() for _ in range(2)]
+        self.k = 0
+
+    def submit(self, x_q, x_scale, topk_ids, topk_w, n_valid, y_host) -> None:
+        i = self.k % 2
+        b = self.bufs[i]
+        if b["x_s"].shape != x_scale.shape:
+            raise ValueError("x_scale shape does not match the layer's scale layout")
+        with torch.cuda.stream(self.h2d):
+            if self.k >= 2:
+                self.h2d.wait_event(self.done[i])      # batch k-2 has read these inputs
+            b["x_q"].copy_(x_q, non_blocking=True)
+            b["x_s"].copy_(x_scale, non_blocking=True)
+            b["ids"].copy_(topk_ids, non_blocking=True)
+            b["w"].copy_(topk_w, non_blocking=True)
+            b["nv"].copy_(n_valid, non_blocking=True)
+            self.in_ready[i].record(self.h2d)
+        self.comp.wait_event(self.in_ready[i])
+        if self.k >= 2:
+            self.comp.wait_event(self.out_copied[i])   # batch k-2's y has left this buffer
+        self.layer.forward(b["x_q"], b["x_s"], b["ids"], b["w"], b["nv"], stream=self.comp,
+                           out=b["y"])
+        self.done[i].record(self.comp)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.done[i])
+            y_host.copy_(b["y"], non_blocking=True)
+            self.out_copied[i].record(self.d2h)
+        self.k += 1
+
+    def synchronize(self) -> None:
+        self.h2d.synchronize()
+        self.comp.synchronize()
+        self.d2h.synchronize()

@@ -371,3 +371,35 @@ def test_empty_and_all_inactive(mx):
     torch.cuda.synchronize()
     assert torch.isnan(y.float()).all()
     assert int(layer.lay.total.item()) == 0
+
+
+def test_host_pipeline_matches_forward(mx, cases):
+    """HostPipeline (pinned host batches, copies on side streams, double
+    buffers) gives every batch's forward output: four batches with different
+    routings through the same two buffer sets."""
+    c = cases["mid_zipf_ragged"]
+    cfg, g = c["cfg"], c["g"]
+    layer = _layer(mx, c)
+    rng = np.random.default_rng(5)
+    batches = []
+    for b in range(4):
+        ids = g["topk_ids"].cpu().numpy().copy()
+        rng.shuffle(ids)  # a different token -> experts assignment per batch
+        batches.append(dict(x_q=g["x_q"].cpu().pin_memory(), x_s=g["x_s"].cpu().pin_memory(),
+                            ids=torch.from_numpy(ids).pin_memory(),
+                            w=g["topk_w"].cpu().pin_memory(),
+                            nv=torch.tensor([c["inp"]["n_valid"]], dtype=torch.int32).pin_memory()))
+    want = []
+    for bt in batches:
+        y = layer.forward(bt["x_q"].cuda(), bt["x_s"].cuda(), bt["ids"].cuda(), bt["w"].cuda(),
+                          bt["nv"].cuda())
+        want.append(y.cpu().clone())
+    pipe = mx.HostPipeline(layer)
+    outs = [torch.zeros(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory() for _ in batches]
+    for bt, o in zip(batches, outs):
+        pipe.submit(bt["x_q"], bt["x_s"], bt["ids"], bt["w"], bt["nv"], o)
+    pipe.synchronize()
+    nv = c["inp"]["n_valid"]
+    for k in range(len(batches)):
+        assert torch.equal(outs[k][:nv], want[k][:nv]), k
+    assert layer.status.item() == 0
