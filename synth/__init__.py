@@ -108,6 +108,12 @@ PARITY_CONFIGS = (
                 seed=14, routing="uniform", n_valid=150, garbage_tail=True),
     LayerConfig("small_h384", T=96, H=384, I=128, E=6, K=2, align=8, seed=15,
                 routing="uniform", inactive_frac=0.10),
+    # many experts (per-expert tables past the GEMM's shared-memory copy),
+    # top-12 (not a power of two), most experts with a single short segment
+    LayerConfig("wide_e160_k12", T=96, H=512, I=256, E=160, K=12, align=32, seed=16,
+                routing="zipf", zipf_s=1.2, zipf_zero_experts=20, inactive_frac=0.05),
+    LayerConfig("wide_e160_k12_ue8m0", T=80, H=512, I=256, E=160, K=12, align=16, seed=17,
+                routing="uniform", scale_mode=SCALE_UE8M0),
 )
 
 
