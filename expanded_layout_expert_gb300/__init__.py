@@ -233,10 +233,16 @@ class ExpandedMoELayer:
     down_proj output rows; the combine sums unweighted.
     weighting "gather": the do_expand=False arrangement (ep_gather): no fold,
     the combine multiplies each pair's row by its weight while summing.
+    masked_max_m: the decode variant. Between the GEMMs each expert's rows
+    sit in a fixed-height slab of masked_max_m rows (moe_expand_to_masked_slab
+    / moe_masked_slab_to_expand); the weight multiplies each pair's down row
+    on the way back (no fold); an expert with more rows than masked_max_m
+    drops the extra ones and flags the status word.
     """
 
     def __init__(self, w13, s13, w2, s2, *, K: int, align: int, scale_mode: str,
-                 max_tokens: int, device=None, weighting: str = "expanded"):
+                 max_tokens: int, device=None, weighting: str = "expanded",
+                 masked_max_m: Optional[int] = None):
         self.w13, self.s13, self.w2, self.s2 = w13, s13, w2, s2
         self.E, twoI, self.H = w13.shape
         self.I = twoI // 2
@@ -245,8 +251,11 @@ class ExpandedMoELayer:
         self.sl = scale_layout_of(scale_mode)
         if weighting not in ("expanded", "gather"):
             raise ValueError(f"weighting must be 'expanded' or 'gather', got {weighting!r}")
+        if masked_max_m is not None and weighting != "expanded":
+            raise ValueError("the masked-slab path weights rows after the slab; use the default weighting")
         self.weighting = weighting
-        if weighting == "gather":
+        self.masked_max_m = masked_max_m
+        if weighting == "gather" or masked_max_m is not None:
             self.flags = 0
         else:
             self.flags = MOE_WEIGHT_OUTPUT_ROWS if scale_mode == "ue8m0" else MOE_FOLD_WEIGHT_INTO_SCALE
@@ -272,6 +281,22 @@ class ExpandedMoELayer:
         self.down_in_scale = new_scale(M, I // 128, self.sl, dev)
         self.down_out = torch.zeros(M, H, dtype=torch.bfloat16, device=dev)
         self.y = torch.zeros(max_tokens, H, dtype=torch.bfloat16, device=dev)
+        if masked_max_m is not None:
+            # decode variant: fixed-height per-expert slabs between the GEMMs
+            S = E * masked_max_m
+            self.slab = torch.zeros(S, H, dtype=torch.uint8, device=dev)
+            self.slab_scale = new_scale(S, H // 128, self.sl, dev)
+            self.masked_m = torch.zeros(E, dtype=torch.int32, device=dev)
+            self.slab_lay = Layout(psum=self.masked_m,
+                                   start=torch.zeros(E, dtype=torch.int32, device=dev),
+                                   total=torch.zeros(1, dtype=torch.int32, device=dev),
+                                   m_indices=torch.zeros(0, dtype=torch.int32, device=dev),
+                                   src2dst=torch.zeros(0, dtype=torch.int32, device=dev),
+                                   tile_prefix=torch.zeros(E + 1, dtype=torch.int32, device=dev),
+                                   E=E, align=1, M_cap=S)
+            self.slab_di = torch.zeros(S, I, dtype=torch.uint8, device=dev)
+            self.slab_di_scale = new_scale(S, I // 128, self.sl, dev)
+            self.slab_out = torch.zeros(S, H, dtype=torch.bfloat16, device=dev)
 
     def forward(self, x_q, x_scale, topk_ids, topk_w, n_valid=None, stream=None,
                 out: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -296,6 +321,17 @@ class ExpandedMoELayer:
                                    self.align, self.M_cap, _ptr(self.xe), _ptr(self.xe_scale),
                                    self.xe_scale.shape[1], _ptr(self.row_w), _ptr(self.status),
                                    s), "moe_expand_scatter")
+        if self.masked_max_m is not None:
+            self._slab_ffn(L, s)
+        else:
+            self._expanded_ffn(L, s)
+        gather_w = self.row_w if self.weighting == "gather" else None
+        check(L.moe_combine(_ptr(self.down_out), _ptr(lay.src2dst), _ptr(gather_w), _ptr(n_valid),
+                            T, self.H, self.K, _ptr(y), s), "moe_combine")
+        return y
+
+    def _expanded_ffn(self, L, s):
+        lay = self.lay
         check(L.moe_grouped_ffn(_ptr(self.xe), _ptr(self.xe_scale), self.xe_scale.shape[1],
                                 self.sl, _ptr(lay.start), _ptr(lay.tile_prefix), _ptr(lay.total),
                                 _ptr(self.w13), _ptr(self.s13), _ptr(self.w2), _ptr(self.s2),
@@ -303,10 +339,34 @@ class ExpandedMoELayer:
                                 None, _ptr(self.down_in), _ptr(self.down_in_scale),
                                 self.down_in_scale.shape[1], _ptr(self.down_out),
                                 _ptr(self.status), s), "moe_grouped_ffn")
-        gather_w = self.row_w if self.weighting == "gather" else None
-        check(L.moe_combine(_ptr(self.down_out), _ptr(lay.src2dst), _ptr(gather_w), _ptr(n_valid),
-                            T, self.H, self.K, _ptr(y), s), "moe_combine")
-        return y
+
+    def _slab_ffn(self, L, s):
+        """Decode variant: expanded rows -> masked slab, both GEMMs on the slab
+        (gate_up with act+quant fused), slab -> expanded rows with the top-k
+        weights."""
+        lay, sl_lay = self.lay, self.slab_lay
+        E, H, I, m = self.E, self.H, self.I, self.masked_max_m
+        S = E * m
+        check(L.moe_expand_to_masked_slab(
+            _ptr(self.xe), _ptr(self.xe_scale), self.sl, self.xe_scale.shape[1], _ptr(lay.psum),
+            _ptr(lay.start), E, H, m, _ptr(self.slab), _ptr(self.slab_scale),
+            self.slab_scale.shape[1], _ptr(self.masked_m), _ptr(sl_lay.start),
+            _ptr(sl_lay.tile_prefix), _ptr(sl_lay.total), _ptr(self.status), s),
+            "moe_expand_to_masked_slab")
+        check(L.moe_grouped_gemm_act_quant(
+            _ptr(self.slab), _ptr(self.slab_scale), self.sl, self.slab_scale.shape[1],
+            _ptr(sl_lay.start), _ptr(sl_lay.tile_prefix), _ptr(sl_lay.total), _ptr(self.w13),
+            _ptr(self.s13), None, 0, E, I, H, S, _ptr(self.slab_di), _ptr(self.slab_di_scale),
+            self.slab_di_scale.shape[1], _ptr(self.status), s), "moe_grouped_gemm_act_quant")
+        check(L.moe_grouped_gemm(
+            _ptr(self.slab_di), _ptr(self.slab_di_scale), self.sl, self.slab_di_scale.shape[1],
+            _ptr(sl_lay.start), _ptr(sl_lay.tile_prefix), _ptr(sl_lay.total), _ptr(self.w2),
+            _ptr(self.s2), None, 0, E, H, I, S, _ptr(self.slab_out), _ptr(self.status), s),
+            "moe_grouped_gemm")
+        check(L.moe_masked_slab_to_expand(
+            _ptr(self.slab_out), m, _ptr(lay.psum), _ptr(lay.start), _ptr(lay.total),
+            _ptr(self.row_w), E, H, self.M_cap, _ptr(self.down_out), s),
+            "moe_masked_slab_to_expand")
 
     @property
     def gateup(self) -> torch.Tensor:

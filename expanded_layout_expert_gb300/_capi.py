@@ -57,6 +57,9 @@ SIGNATURES = {
     "moe_grouped_ffn": (I32, [P, P, I64, I32, P, P, P, P, P, P, P, P, I32, I32, I32, I32, I64,
                               P, P, P, I64, P, P, P]),
     "moe_combine": (I32, [P, P, P, P, I64, I32, I32, P, P]),
+    "moe_expand_to_masked_slab": (I32, [P, P, I32, I64, P, P, I32, I32, I64, P, P, I64, P, P, P,
+                                        P, P, P]),
+    "moe_masked_slab_to_expand": (I32, [P, I64, P, P, P, P, I32, I32, I64, P, P]),
     "moe_gemm_set_trace": (I32, [P]),
     "moe_last_error_string": (C.c_char_p, []),
     "moe_device_supported": (I32, [I32]),

@@ -259,6 +259,40 @@ int moe_combine(const uint16_t* down_out, const int32_t* src2dst, const float* r
                 const int32_t* d_n_valid, int64_t T, int H, int K, uint16_t* y,
                 moe_stream_t stream);
 
+/*
+ * Decode variant, before the GEMMs: expanded rows -> masked slab (SGLang PR
+ * 37261: the deepep_v2 decode path's expand_to_masked_slab, feeding a masked
+ * grouped GEMM with a fixed-height slab [E, max_m, H]). Expert e's first
+ * masked_m[e] = min(count_e, max_m) expanded rows (count_e = psum[e] -
+ * start[e]) go to slab rows e*max_m + j with their scale rows; slab rows
+ * [masked_m[e], round_up(masked_m[e], 128)) below max_m are zeroed; other
+ * slab rows are not touched. count_e > max_m drops the extra rows and sets
+ * MOE_ERR_DEVICE_CHECK on d_status. Also writes the layout the grouped GEMMs
+ * take for the slab: slab_start[e] = e*max_m, slab_tile_prefix [E+1] (128-row
+ * tiles of masked_m), *slab_total = E*max_m; pass M_cap = E*max_m to them.
+ *   xe, xe_scale (ld_xes), psum, start: from moe_expand_scatter / layout
+ *   slab     device uint8 [E*max_m, H]; slab_scale fp32 [E*max_m, ld_ss] or
+ *            packed ue8m0 int32 [ceil(H/512), ld_ss >= E*max_m]
+ *   masked_m, slab_start device int32 [E]; slab_tile_prefix [E+1]; slab_total [1]
+ */
+int moe_expand_to_masked_slab(const uint8_t* xe, const void* xe_scale, int scale_layout,
+                              int64_t ld_xes, const int32_t* psum, const int32_t* start, int E,
+                              int H, int64_t max_m, uint8_t* slab, void* slab_scale, int64_t ld_ss,
+                              int32_t* masked_m, int32_t* slab_start, int32_t* slab_tile_prefix,
+                              int32_t* slab_total, int32_t* d_status, moe_stream_t stream);
+
+/*
+ * Decode variant, after the GEMMs: masked slab -> expanded rows (the decode
+ * path's masked_slab_to_expand, which takes the top-k weights):
+ *   out[start[e] + j] = bf16( f32(slab_out[e*max_m + j]) * (row_w ? row_w[start[e]+j] : 1) )
+ * for j < min(count_e, max_m); every other row below *d_total is zeroed
+ * (alignment gaps, dropped rows); rows >= *d_total are not written.
+ *   slab_out device bf16 [E*max_m, H] (H % 8 == 0); out bf16 [M_cap, H]
+ */
+int moe_masked_slab_to_expand(const uint16_t* slab_out, int64_t max_m, const int32_t* psum,
+                              const int32_t* start, const int32_t* d_total, const float* row_w,
+                              int E, int H, int64_t M_cap, uint16_t* out, moe_stream_t stream);
+
 /* Host. Diagnostics: when d_trace is not NULL, every later moe_grouped_gemm
  * launch writes 8 uint64 counters per CTA (grid = SM count) to d_trace:
  * kernel cycles, producer cycles waiting for a free stage, MMA cycles waiting

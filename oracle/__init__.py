@@ -287,8 +287,12 @@ def run_layer(inp: dict, M_cap: int, weighting: str = "expanded") -> dict:
     weighting "gather": the do_expand=False arrangement of the same PR's A/B
     baseline, where ep_gather applies the weights while summing
     (post_permute_deep_gemm_to_deepep_v2's non-expanded branch): no fold, no
-    row weighting, y[t] = bf16(sum_k w[t,k] * down[row(t,k)])."""
-    if weighting not in ("expanded", "gather"):
+    row weighting, y[t] = bf16(sum_k w[t,k] * down[row(t,k)]).
+    weighting "rows": the decode masked-slab arrangement (masked_slab_to_expand
+    takes the top-k weights): no fold on either scale layout, every down row
+    multiplied by its weight and rounded to bf16, then the unweighted sum.
+    On the ue8m0 path it is the same as "expanded"."""
+    if weighting not in ("expanded", "gather", "rows"):
         raise ValueError(weighting)
     cfg = inp["cfg"]
     sl = inp["scale_layout"]
@@ -307,6 +311,11 @@ def run_layer(inp: dict, M_cap: int, weighting: str = "expanded") -> dict:
         di, di_s = act_quant_rows(gu, None, sl)
         down = gemm_rows(di, di_s, sl, di_s.shape[1], rows, experts, inp["w2"], inp["s2"])
         y = combine(down, lay["src2dst"], row_w, nv, T)
+    elif weighting == "rows":
+        di, di_s = act_quant_rows(gu, None, sl)
+        down_u = gemm_rows(di, di_s, sl, di_s.shape[1], rows, experts, inp["w2"], inp["s2"])
+        down = weight_rows(down_u, row_w[:total])
+        y = combine(down, lay["src2dst"], None, nv, T)
     else:
         if sl == SCALE_F32:
             di, di_s = act_quant_rows(gu, row_w[:total], sl)

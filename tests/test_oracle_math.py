@@ -273,3 +273,33 @@ def test_gather_layer_equals_sum_of_weighted_single_pair_paths(orc, layer_runs):
             one["topk_w"] = unit
             acc += float(w[t, k]) * orc.bf16_decode(orc.token_forward(one, t))
         assert np.array_equal(orc.bf16_encode(acc), g["y"][t]), t
+
+
+def test_rows_weighting_pins(orc, layer_runs):
+    """The decode arrangement (each down row weighted and rounded, then an
+    unweighted sum): on ue8m0 it is the expanded layer itself; on fp32 scales
+    it is, token by token, bf16(sum_k bf16(w_k * f(x_t, e_k))) with f the
+    unweighted pair path, and its codes are the gather arrangement's."""
+    inp, out, M_cap = layer_runs["mid_ue8m0"]
+    r = orc.run_layer(inp, M_cap, weighting="rows")
+    assert np.array_equal(r["y"], out["y"])
+    inp, out, M_cap = layer_runs["tiny_h512"]
+    r = orc.run_layer(inp, M_cap, weighting="rows")
+    g = orc.run_layer(inp, M_cap, weighting="gather")
+    assert np.array_equal(r["di"], g["di"]) and np.array_equal(r["di_s"], g["di_s"])
+    ids, w = inp["topk_ids"], inp["topk_w"]
+    for t in range(0, 12):
+        acc = np.zeros(inp["x_q"].shape[1])
+        for k in range(ids.shape[1]):
+            if ids[t, k] < 0:
+                continue
+            one = dict(inp)
+            only = -np.ones_like(ids)
+            only[t, k] = ids[t, k]
+            one["topk_ids"] = only
+            unit = inp["topk_w"].copy()
+            unit[t, k] = 1.0
+            one["topk_w"] = unit
+            f = orc.bf16_decode(orc.token_forward(one, t))
+            acc += orc.bf16_decode(orc.bf16_encode(f * float(w[t, k])))
+        assert np.array_equal(orc.bf16_encode(acc), r["y"][t]), t
