@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--weighting", choices=["expanded", "gather"], default="expanded",
                     help="expanded: fold / output-row weighting (do_expand=True); gather: "
                          "weights applied in the combine (the do_expand=False A/B arrangement)")
+    ap.add_argument("--masked-max-m", type=int, default=0,
+                    help="decode variant: both GEMMs on per-expert slabs of this height")
     ap.add_argument("--unfused", action="store_true",
                     help="run gate_up and act+quant as two launches")
     ap.add_argument("--gemm-tile-n128", action="store_true",
@@ -207,7 +209,8 @@ def run_ours(args, world, rank, local):
     nv = d["n_valid"]
     n_valid = torch.tensor([nv], dtype=torch.int32, device=dev)
     layer = mx.ExpandedMoELayer(d["w13"], d["s13"], d["w2"], d["s2"], K=cfg.K, align=cfg.align,
-                                scale_mode=cfg.scale_mode, max_tokens=cfg.T, weighting=args.weighting)
+                                scale_mode=cfg.scale_mode, max_tokens=cfg.T, weighting=args.weighting,
+                                masked_max_m=args.masked_max_m or None)
     L = mx.load()
     stream = torch.cuda.current_stream()
     s = stream.cuda_stream
@@ -238,6 +241,37 @@ def run_ours(args, world, rank, local):
                                       ptr(layer.xe), ptr(layer.xe_scale), layer.xe_scale.shape[1],
                                       ptr(layer.row_w), ptr(layer.status), s), "scatter")
         mark(2)
+        if layer.masked_max_m is not None:
+            # decode variant: slab in, fused gate_up on the slab (segment
+            # gemm1), down on the slab and back to expanded rows (gemm2)
+            E, mm = cfg.E, layer.masked_max_m
+            S = E * mm
+            sll = layer.slab_lay
+            mx.check(L.moe_expand_to_masked_slab(
+                ptr(layer.xe), ptr(layer.xe_scale), layer.sl, layer.xe_scale.shape[1],
+                ptr(lay.psum), ptr(lay.start), E, cfg.H, mm, ptr(layer.slab), ptr(layer.slab_scale),
+                layer.slab_scale.shape[1], ptr(layer.masked_m), ptr(sll.start), ptr(sll.tile_prefix),
+                ptr(sll.total), ptr(layer.status), s), "slab")
+            mx.check(L.moe_grouped_gemm_act_quant(
+                ptr(layer.slab), ptr(layer.slab_scale), layer.sl, layer.slab_scale.shape[1],
+                ptr(sll.start), ptr(sll.tile_prefix), ptr(sll.total), ptr(layer.w13), ptr(layer.s13),
+                None, 0, E, cfg.I, cfg.H, S, ptr(layer.slab_di), ptr(layer.slab_di_scale),
+                layer.slab_di_scale.shape[1], ptr(layer.status), s), "gemm1+act_quant (slab)")
+            mark(3)
+            mark(4)
+            mx.check(L.moe_grouped_gemm(
+                ptr(layer.slab_di), ptr(layer.slab_di_scale), layer.sl, layer.slab_di_scale.shape[1],
+                ptr(sll.start), ptr(sll.tile_prefix), ptr(sll.total), ptr(layer.w2), ptr(layer.s2),
+                None, 0, E, cfg.H, cfg.I, S, ptr(layer.slab_out), ptr(layer.status), s),
+                "gemm2 (slab)")
+            mx.check(L.moe_masked_slab_to_expand(
+                ptr(layer.slab_out), mm, ptr(lay.psum), ptr(lay.start), ptr(lay.total),
+                ptr(layer.row_w), E, cfg.H, layer.M_cap, ptr(layer.down_out), s), "unslab")
+            mark(5)
+            mx.check(L.moe_combine(ptr(layer.down_out), ptr(lay.src2dst), None, ptr(n_valid), cfg.T,
+                                   cfg.H, cfg.K, ptr(layer.y), s), "combine")
+            mark(6)
+            return
         if fused:
             mx.check(L.moe_grouped_gemm_act_quant(
                 ptr(layer.xe), ptr(layer.xe_scale), layer.sl, layer.xe_scale.shape[1],
@@ -343,6 +377,7 @@ def run_ours(args, world, rank, local):
                                if cfg.routing == "zipf" else cfg.routing),
                    "inactive_rows": cfg.inactive_frac, "scales": cfg.scale_mode,
                    "weighting": args.weighting,
+                   "masked_max_m": args.masked_max_m or None,
                    "valid_pairs": P, "expanded_rows": M_pad, "M_cap": layer.M_cap,
                    "l2": "flushed between steps (256 MiB write outside the timed events)",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
@@ -355,7 +390,7 @@ def run_ours(args, world, rank, local):
                      "unit": "TFLOP/s", "frac": kernels["gemm1"]["frac"],
                      "traffic": GATE_UP_DRAM_BYTES.get(cfg.name) if fused else None,
                      "peak_source": f"{peak_src}: bf16 burst x {FP8_PER_BF16:g} (nominal fp8:bf16)"},
-        "gpu_launches": (6 if fused else 7) * args.steps,
+        "gpu_launches": (8 if args.masked_max_m else (6 if fused else 7)) * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": round(t_wall, 3),
     }
