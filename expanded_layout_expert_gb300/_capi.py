@@ -61,6 +61,7 @@ SIGNATURES = {
                                         P, P, P]),
     "moe_masked_slab_to_expand": (I32, [P, I64, P, P, P, P, I32, I32, I64, P, P]),
     "moe_gemm_set_trace": (I32, [P]),
+    "moe_selftest_bounded_wait": (I32, [I64, P, P, P]),
     "moe_last_error_string": (C.c_char_p, []),
     "moe_device_supported": (I32, [I32]),
 }

@@ -65,13 +65,14 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits until the phase with the given parity has completed. Gives up when
 // *abort becomes non-zero (another role gave up) or after kWaitLimitCycles,
 // in which case it records MOE_ERR_TIMEOUT, raises *abort and returns false.
-MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status) {
+MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status,
+                       long long limit_cycles = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit_cycles) {
       *abort = 1;
       set_status(status, MOE_ERR_TIMEOUT);
       return false;

@@ -344,6 +344,31 @@ def test_device_checks_report_without_faulting(mx):
     assert ((s2d == -1) | (s2d < 16)).all()
 
 
+def test_bounded_wait_times_out_and_the_context_survives(mx, cases):
+    """A wait on a barrier nothing arrives at gives up after its limit with
+    MOE_ERR_TIMEOUT on the status word; a second role leaves on the abort
+    flag well before its own (longer) limit; the device keeps working."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((4,), -1, dtype=torch.int64, device="cuda")
+    limit = 2_000_000  # about 1 ms
+    mx.check(mx.load().moe_selftest_bounded_wait(limit, status.data_ptr(), out.data_ptr(),
+                                                  torch.cuda.current_stream().cuda_stream),
+             "selftest")
+    torch.cuda.synchronize()
+    o = out.cpu().tolist()
+    assert status.item() == mx._capi.MOE_ERR_TIMEOUT
+    assert o[0] == 0 and o[1] >= limit
+    assert o[2] == 0 and o[3] < 4 * limit, "the second waiter left on the abort flag"
+    # the context is still usable: a whole layer runs and matches the oracle
+    c = cases["tiny_h512"]
+    g = c["g"]
+    layer = _layer(mx, c)
+    y = layer.forward(g["x_q"], g["x_s"], g["topk_ids"], g["topk_w"], g["n_valid_dev"])
+    torch.cuda.synchronize()
+    nv = c["inp"]["n_valid"]
+    assert_final_close(u16(y)[:nv], c["ref"]["y"][:nv], "after timeout")
+
+
 def test_empty_and_all_inactive(mx):
     E, K, T, H, I = 4, 2, 6, 256, 128
     dev = "cuda"
