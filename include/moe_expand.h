@@ -293,12 +293,16 @@ int moe_masked_slab_to_expand(const uint16_t* slab_out, int64_t max_m, const int
                               const int32_t* start, const int32_t* d_total, const float* row_w,
                               int E, int H, int64_t M_cap, uint16_t* out, moe_stream_t stream);
 
-/* Host. Diagnostics: when d_trace is not NULL, every later moe_grouped_gemm
- * launch writes 8 uint64 counters per CTA (grid = SM count) to d_trace:
- * kernel cycles, producer cycles waiting for a free stage, MMA cycles waiting
- * for a free accumulator, MMA cycles waiting for operand data, three unused
- * words, and K blocks processed. NULL turns it off. Not thread-safe with
- * respect to concurrent launches on other threads. */
+/* Host. Diagnostics: when d_trace is not NULL, every later grouped-GEMM
+ * launch (moe_grouped_gemm, moe_grouped_gemm_act_quant) writes 8 uint64
+ * counters per CTA (grid = SM count) to d_trace: kernel cycles, producer
+ * cycles waiting for a free stage, MMA cycles waiting for a free accumulator,
+ * MMA cycles waiting for operand data, then (per-K-block promotion kernel)
+ * epilogue cycles waiting for an accumulator, epilogue cycles in tile-end
+ * work, one unused word, or (block-scaled kernel) MMA cycles waiting for
+ * scales, epilogue wait, epilogue tile work; last, K blocks processed. NULL
+ * turns it off. Not thread-safe with respect to concurrent launches on other
+ * threads. */
 int moe_gemm_set_trace(uint64_t* d_trace);
 
 /* Diagnostics (no counterpart in the pages): runs the library's bounded

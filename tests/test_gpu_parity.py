@@ -344,6 +344,27 @@ def test_device_checks_report_without_faulting(mx):
     assert ((s2d == -1) | (s2d < 16)).all()
 
 
+@pytest.mark.parametrize("name", ["mid_f32", "mid_ue8m0_ragged", "wide_e160_k12"])
+def test_grouped_ffn_fused_equals_three_launches(mx, cases, name):
+    """moe_grouped_ffn's default (gate_up with act+quant fused) and its
+    MOE_FFN_UNFUSED three-launch path give the same down_proj output bits."""
+    c = cases[name]
+    g = c["g"]
+    lay = _gpu_layout(mx, c)
+    xe, xe_s, row_w = mx.expand_scatter(g["x_q"], g["x_s"], c["sl"], g["topk_w"], lay,
+                                        n_valid=g["n_valid_dev"])
+    flags = mx.MOE_FOLD_WEIGHT_INTO_SCALE if c["sl"] == 0 else mx.MOE_WEIGHT_OUTPUT_ROWS
+    outs = []
+    for extra in (0, mx.MOE_FFN_UNFUSED):
+        _, di, di_s, down = mx.grouped_ffn(xe, xe_s, c["sl"], lay, g["w13"], g["s13"], g["w2"],
+                                           g["s2"], row_w, flags | extra)
+        outs.append((di, di_s, down))
+    torch.cuda.synchronize()
+    tot = c["ref"]["total"]
+    assert torch.equal(outs[0][0][:tot], outs[1][0][:tot])
+    assert torch.equal(outs[0][2][:tot].view(torch.int16), outs[1][2][:tot].view(torch.int16))
+
+
 def test_bounded_wait_times_out_and_the_context_survives(mx, cases):
     """A wait on a barrier nothing arrives at gives up after its limit with
     MOE_ERR_TIMEOUT on the status word; a second role leaves on the abort
@@ -398,13 +419,19 @@ def test_empty_and_all_inactive(mx):
     assert int(layer.lay.total.item()) == 0
 
 
-def test_host_pipeline_matches_forward(mx, cases):
+@pytest.mark.parametrize("mode", ["expanded", "gather", "masked"])
+def test_host_pipeline_matches_forward(mx, cases, mode):
     """HostPipeline (pinned host batches, copies on side streams, double
     buffers) gives every batch's forward output: four batches with different
-    routings through the same two buffer sets."""
+    routings through the same two buffer sets, for each layer arrangement."""
     c = cases["mid_zipf_ragged"]
     cfg, g = c["cfg"], c["g"]
-    layer = _layer(mx, c)
+    if mode == "masked":
+        layer = mx.ExpandedMoELayer(g["w13"], g["s13"], g["w2"], g["s2"], K=cfg.K,
+                                    align=cfg.align, scale_mode=cfg.scale_mode,
+                                    max_tokens=cfg.T, masked_max_m=cfg.T * cfg.K)
+    else:
+        layer = _layer(mx, c, weighting=mode)
     rng = np.random.default_rng(5)
     batches = []
     for b in range(4):
