@@ -25,11 +25,17 @@
 //  - warps 2-3 are spare; with BN = 256 warpgroup 0 hands its registers to
 //    the epilogue warpgroups (setmaxnreg). Scale words are loaded two
 //    K blocks before use and decoded only then, so no global load is waited
-//    for early. At the end of the tile it converts to bf16 and stores its row.
+//    for early. At the end of the tile it converts to bf16 and stores its row
+//    (Staged: through shared memory, whole 128-byte rows per instruction; used
+//    for short-K GEMMs, where the store is a larger share of a tile).
+//  - Fused (moe_grouped_gemm_act_quant): the tile pairs gate and up columns
+//    and the epilogue applies silu*mul, the fp8 quantiser and the weight fold
+//    instead of storing bf16 (see the kernel's comment).
 // The m-tiles come from the layout's per-expert tile prefix, read on the
 // device: a CTA maps a linear tile id to (expert, m block, n block), and
 // tiles past the device-side total are never visited, so a capacity-sized
-// buffer costs nothing beyond its real rows.
+// buffer costs nothing beyond its real rows. moe_grouped_gemm sends ue8m0
+// scales with N % 256 == 0 to the block-scaled kernel (grouped_gemm_mx.cu).
 #include <cuda_bf16.h>
 
 #include <atomic>
