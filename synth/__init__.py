@@ -114,6 +114,10 @@ PARITY_CONFIGS = (
                 routing="zipf", zipf_s=1.2, zipf_zero_experts=20, inactive_frac=0.05),
     LayerConfig("wide_e160_k12_ue8m0", T=80, H=512, I=256, E=160, K=12, align=16, seed=17,
                 routing="uniform", scale_mode=SCALE_UE8M0),
+    # ue8m0 with H % 256 != 0: the down GEMM takes 128-column tiles and the
+    # per-K-block promotion kernel
+    LayerConfig("small_h384_ue8m0", T=64, H=384, I=128, E=6, K=2, align=8, seed=18,
+                routing="uniform", scale_mode=SCALE_UE8M0, inactive_frac=0.10),
 )
 
 
