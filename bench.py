@@ -64,6 +64,8 @@ def parse_args(argv=None):
                          "weights applied in the combine (the do_expand=False A/B arrangement)")
     ap.add_argument("--masked-max-m", type=int, default=0,
                     help="decode variant: both GEMMs on per-expert slabs of this height")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of a CUDA graph of the whole forward (no per-kernel split)")
     ap.add_argument("--unfused", action="store_true",
                     help="run gate_up and act+quant as two launches")
     ap.add_argument("--gemm-tile-n128", action="store_true",
@@ -313,6 +315,19 @@ def run_ours(args, world, rank, local):
     if layer.status.item() != 0:
         raise RuntimeError(f"device status {layer.status.item()} after warm-up")
 
+    if args.graph:
+        cap = layer.capture(x_q, x_s, ids, w, n_valid)
+        cap.replay()
+        torch.cuda.synchronize()
+
+        def step(ev=None):  # noqa: F811  (the whole layer as one graph launch)
+            if ev is not None:
+                for i in range(6):
+                    ev[i].record(stream)
+            cap.replay()
+            if ev is not None:
+                ev[6].record(stream)
+
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
@@ -349,7 +364,7 @@ def run_ours(args, world, rank, local):
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     fp8_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * FP8_PER_BF16
     kernels = {}
-    for n in names:
+    for n in ([] if args.graph else names):
         ms = per_kernel[n]
         if fused and n == "act_quant":
             kernels[n] = {"ms": 0.0, "fused_into": "gemm1"}
@@ -362,9 +377,20 @@ def run_ours(args, world, rank, local):
             ach = work[n] / (ms / 1e3) / 1e9
             kernels[n] = {"ms": round(ms, 4), "achieved": round(ach, 1), "unit": "GB/s",
                           "frac": round(ach / hbm, 4), "work": work[n]}
-    sc_bytes = work["scatter"] + work["combine"]
-    sc_gbs = sc_bytes / ((per_kernel["scatter"] + per_kernel["combine"]) / 1e3) / 1e9
-    gemm_tflops = (work["gemm1"] + work["gemm2"]) / ((per_kernel["gemm1"] + per_kernel["gemm2"]) / 1e3) / 1e12
+    if args.graph:
+        kernels = {"graph_replay": {"ms": round(step_ms, 4)}}
+        sc_gbs = gemm_tflops = float("nan")
+        roofline = None
+    else:
+        sc_bytes = work["scatter"] + work["combine"]
+        sc_gbs = sc_bytes / ((per_kernel["scatter"] + per_kernel["combine"]) / 1e3) / 1e9
+        gemm_tflops = (work["gemm1"] + work["gemm2"]) / ((per_kernel["gemm1"] + per_kernel["gemm2"]) / 1e3) / 1e12
+        roofline = {"bound": "tensor",
+                    "kernel": "grouped_gemm (gate_up" + (" + act_quant epilogue)" if fused else ")"),
+                    "achieved": kernels["gemm1"]["achieved"], "peak": round(fp8_peak, 1),
+                    "unit": "TFLOP/s", "frac": kernels["gemm1"]["frac"],
+                    "traffic": GATE_UP_DRAM_BYTES.get(cfg.name) if fused else None,
+                    "peak_source": f"{peak_src}: bf16 burst x {FP8_PER_BF16:g} (nominal fp8:bf16)"}
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -378,18 +404,14 @@ def run_ours(args, world, rank, local):
                    "inactive_rows": cfg.inactive_frac, "scales": cfg.scale_mode,
                    "weighting": args.weighting,
                    "masked_max_m": args.masked_max_m or None,
+                   "cuda_graph": bool(args.graph),
                    "valid_pairs": P, "expanded_rows": M_pad, "M_cap": layer.M_cap,
                    "l2": "flushed between steps (256 MiB write outside the timed events)",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
-        "scatter_combine_gbs": round(sc_gbs, 1),
-        "grouped_fp8_tflops": round(gemm_tflops, 1),
+        "scatter_combine_gbs": None if args.graph else round(sc_gbs, 1),
+        "grouped_fp8_tflops": None if args.graph else round(gemm_tflops, 1),
         "kernels": kernels,
-        "roofline": {"bound": "tensor",
-                     "kernel": "grouped_gemm (gate_up" + (" + act_quant epilogue)" if fused else ")"),
-                     "achieved": kernels["gemm1"]["achieved"], "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": kernels["gemm1"]["frac"],
-                     "traffic": GATE_UP_DRAM_BYTES.get(cfg.name) if fused else None,
-                     "peak_source": f"{peak_src}: bf16 burst x {FP8_PER_BF16:g} (nominal fp8:bf16)"},
+        "roofline": roofline,
         "gpu_launches": (8 if args.masked_max_m else (6 if fused else 7)) * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": round(t_wall, 3),

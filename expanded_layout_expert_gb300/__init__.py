@@ -23,7 +23,7 @@ from ._capi import (MOE_BLOCK_M, MOE_FFN_UNFUSED, MOE_FOLD_WEIGHT_INTO_SCALE, MO
 __all__ = [
     "expanded_capacity", "workspace_size", "expand_layout", "expand_scatter", "grouped_gemm",
     "act_quant", "grouped_gemm_act_quant", "grouped_ffn", "combine", "ExpandedMoELayer",
-    "HostPipeline", "Layout",
+    "HostPipeline", "CapturedForward", "Layout",
     "MoEError",
     "MOE_SCALE_F32_ROWMAJOR", "MOE_SCALE_UE8M0_PACKED_COLMAJOR", "MOE_FOLD_WEIGHT_INTO_SCALE",
     "MOE_WEIGHT_OUTPUT_ROWS", "MOE_GEMM_TILE_N128", "MOE_GEMM_CTA_PAIR",
@@ -368,6 +368,16 @@ class ExpandedMoELayer:
             _ptr(self.row_w), E, H, self.M_cap, _ptr(self.down_out), s),
             "moe_masked_slab_to_expand")
 
+    def capture(self, x_q, x_scale, topk_ids, topk_w, n_valid=None,
+                out: Optional[torch.Tensor] = None) -> "CapturedForward":
+        """Records one forward on these device tensors into a CUDA graph.
+        Replaying it reruns the whole layer (every kernel, no host work) on
+        whatever the tensors hold at replay time: refill them in place, then
+        call replay(). Run one eager forward first so the library has set up
+        its per-device state; the captured launches must not be captured
+        while another capture on the same device is in progress."""
+        return CapturedForward(self, x_q, x_scale, topk_ids, topk_w, n_valid, out)
+
     @property
     def gateup(self) -> torch.Tensor:
         """bf16 [M_cap, 2I] buffer for the stand-alone gate_up GEMM (the
@@ -451,3 +461,25 @@ class HostPipeline:
         self.h2d.synchronize()
         self.comp.synchronize()
         self.d2h.synchronize()
+
+
+class CapturedForward:
+    """A CUDA graph of one ExpandedMoELayer.forward over fixed device tensors
+    (see ExpandedMoELayer.capture). replay() launches the recorded kernels on
+    the current stream and returns the output tensor."""
+
+    def __init__(self, layer: "ExpandedMoELayer", x_q, x_scale, topk_ids, topk_w, n_valid, out):
+        self.layer = layer
+        self.inputs = (x_q, x_scale, topk_ids, topk_w, n_valid)
+        self.out = out if out is not None else layer.y
+        side = torch.cuda.Stream(layer.device)
+        side.wait_stream(torch.cuda.current_stream(layer.device))
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(self.graph, stream=side):
+                layer.forward(x_q, x_scale, topk_ids, topk_w, n_valid, stream=side, out=self.out)
+        torch.cuda.current_stream(layer.device).wait_stream(side)
+
+    def replay(self) -> torch.Tensor:
+        self.graph.replay()
+        return self.out

@@ -5,9 +5,9 @@
 // 54109, Design: kernels must skip inactive rows or make them safe to
 // discard, and never trust row contents).
 //
-// A persistent grid of warps walks the valid tokens, one token per warp at a
-// time; each lane owns 16-byte column vectors (8 bf16) of the row and issues
-// the K gathers for one vector back to back before accumulating.
+// A persistent grid of warps walks (valid token, 256-column chunk) tasks;
+// each lane owns one 16-byte column vector (8 bf16) of the chunk and issues
+// the K gathers for it back to back before accumulating.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -30,62 +30,65 @@ MOE_DEV void acc8(float (&a)[8], const uint4& v, float w) {
 
 constexpr int kThreads = 256;
 
-// One warp per token: lane k < K holds the token's k-th expanded row (and its
-// weight) and broadcasts it by shuffle; each lane then owns 16-byte column
-// vectors of the row, strided by the warp, with the K gathers of one vector
-// issued back to back before they are summed.
+// One warp per (token, 256-column chunk): lane k < K holds the token's k-th
+// expanded row (and its weight) and broadcasts it by shuffle; each lane owns
+// one 16-byte column vector of the chunk, with the K gathers of that vector
+// issued back to back before they are summed. Chunking the row keeps the GPU
+// busy when there are few tokens (a decode batch) as well as many.
 __global__ void __launch_bounds__(kThreads) combine_kernel(
     const uint4* __restrict__ down, const int32_t* __restrict__ src2dst,
     const float* __restrict__ row_w, const int32_t* __restrict__ d_n_valid, int64_t T, int H,
     int K, uint4* __restrict__ y) {
   const int lane = threadIdx.x & 31;
   const int nvec = H / 8;
+  const int nchunk = (nvec + 31) / 32;
   int64_t nv = T;
   if (d_n_valid != nullptr) {
     nv = *d_n_valid;
     nv = nv < 0 ? 0 : (nv > T ? T : nv);
   }
+  const int64_t tasks = nv * nchunk;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5; t < nv;
-       t += nwarps) {
+  for (int64_t task = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+       task < tasks; task += nwarps) {
+    const int64_t t = task / nchunk;
+    const int v = static_cast<int>(task - t * nchunk) * 32 + lane;
     int my_r = -1;
     float my_w = 1.0f;
     if (lane < K) {
       my_r = src2dst[t * K + lane];
       if (my_r >= 0 && row_w != nullptr) my_w = row_w[my_r];
     }
-    // warp-uniform loop (the shuffles need every lane); lanes past the row idle
-    for (int v0 = 0; v0 < nvec; v0 += 32) {
-      const int v = v0 + lane;
-      const bool act = v < nvec;
-      float a[8];
+    // warp-uniform from here (the shuffles need every lane); lanes past the
+    // row idle
+    const bool act = v < nvec;
+    float a[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = 0.0f;
-      for (int k0 = 0; k0 < K; k0 += 4) {
-        uint4 d[4];
-        int r[4];
-        float w[4];
+    for (int i = 0; i < 8; ++i) a[i] = 0.0f;
+    for (int k0 = 0; k0 < K; k0 += 4) {
+      uint4 d[4];
+      int r[4];
+      float w[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          r[j] = __shfl_sync(0xffffffffu, my_r, (k0 + j) & 31);
-          w[j] = __shfl_sync(0xffffffffu, my_w, (k0 + j) & 31);
-          if (k0 + j >= K || !act) r[j] = -1;
-          d[j] = r[j] >= 0 ? __ldcs(down + static_cast<int64_t>(r[j]) * nvec + v)
-                           : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (r[j] >= 0) acc8(a, d[j], w[j]);
+      for (int j = 0; j < 4; ++j) {
+        r[j] = __shfl_sync(0xffffffffu, my_r, (k0 + j) & 31);
+        w[j] = __shfl_sync(0xffffffffu, my_w, (k0 + j) & 31);
+        if (k0 + j >= K || !act) r[j] = -1;
+        d[j] = r[j] >= 0 ? __ldcs(down + static_cast<int64_t>(r[j]) * nvec + v)
+                         : make_uint4(0, 0, 0, 0);
       }
-      uint4 o;
-      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(a[2 * i], a[2 * i + 1]);
-        ow[i] = *reinterpret_cast<const uint32_t*>(&b);
-      }
-      if (act) y[t * nvec + v] = o;
+      for (int j = 0; j < 4; ++j)
+        if (r[j] >= 0) acc8(a, d[j], w[j]);
     }
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(a[2 * i], a[2 * i + 1]);
+      ow[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    if (act) y[t * nvec + v] = o;
   }
 }
 
@@ -102,7 +105,8 @@ extern "C" int moe_combine(const uint16_t* down_out, const int32_t* src2dst, con
   MOE_REQUIRE_DEVICE();
   if (T == 0) return MOE_OK;
   int64_t grid = static_cast<int64_t>(moe::device_sm_count()) * (2048 / moe::kThreads);
-  const int64_t need = (T + (moe::kThreads / 32) - 1) / (moe::kThreads / 32);
+  const int64_t tasks = T * ((H / 8 + 31) / 32);
+  const int64_t need = (tasks + (moe::kThreads / 32) - 1) / (moe::kThreads / 32);
   if (grid > need) grid = need;
   moe::combine_kernel<<<static_cast<unsigned>(grid), moe::kThreads, 0,
                         reinterpret_cast<cudaStream_t>(stream)>>>(

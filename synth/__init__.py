@@ -90,6 +90,13 @@ CONFIGS = (
                 garbage_tail=True),
 )
 
+# A decode-sized batch (not one of the five layer workloads): few tokens per
+# expert, for the masked-slab variant and graph-replay measurements.
+EXTRA_CONFIGS = (
+    LayerConfig("decode_t256_h7168_ue8m0", T=256, H=7168, I=2048, E=64, K=8, align=16,
+                seed=20, routing="uniform", scale_mode=SCALE_UE8M0),
+)
+
 # Shapes small enough for the oracle to run every row in seconds, still
 # spanning several 128-row tiles, several N tiles and ragged tails.
 PARITY_CONFIGS = (
@@ -122,7 +129,7 @@ PARITY_CONFIGS = (
 
 
 def config_by_name(name: str) -> LayerConfig:
-    for c in CONFIGS + PARITY_CONFIGS:
+    for c in CONFIGS + PARITY_CONFIGS + EXTRA_CONFIGS:
         if c.name == name:
             return c
     raise KeyError(name)

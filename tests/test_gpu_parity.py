@@ -365,6 +365,35 @@ def test_grouped_ffn_fused_equals_three_launches(mx, cases, name):
     assert torch.equal(outs[0][2][:tot].view(torch.int16), outs[1][2][:tot].view(torch.int16))
 
 
+@pytest.mark.parametrize("mode", ["expanded", "masked"])
+def test_captured_forward_replays(mx, cases, mode):
+    """A CUDA graph of the whole forward replays to the eager result, and
+    again after the inputs are refilled in place with a new routing."""
+    c = cases["mid_zipf_ragged"]
+    cfg, g = c["cfg"], c["g"]
+    kw = dict(K=cfg.K, align=cfg.align, scale_mode=cfg.scale_mode, max_tokens=cfg.T)
+    if mode == "masked":
+        kw["masked_max_m"] = cfg.T * cfg.K
+    layer = mx.ExpandedMoELayer(g["w13"], g["s13"], g["w2"], g["s2"], **kw)
+    x_q, x_s = g["x_q"].clone(), g["x_s"].clone()
+    ids, w, nv = g["topk_ids"].clone(), g["topk_w"].clone(), g["n_valid_dev"].clone()
+    want0 = layer.forward(x_q, x_s, ids, w, nv).clone()
+    out = torch.zeros_like(layer.y)
+    cap = layer.capture(x_q, x_s, ids, w, nv, out=out)
+    y = cap.replay()
+    torch.cuda.synchronize()
+    n = c["inp"]["n_valid"]
+    assert torch.equal(y[:n], want0[:n])
+    perm = torch.randperm(cfg.T, generator=torch.Generator().manual_seed(3))
+    ids.copy_(g["topk_ids"][perm.cuda()])
+    want1 = layer.forward(x_q, x_s, ids, w, nv).clone()
+    y = cap.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y[:n], want1[:n])
+    assert not torch.equal(want0[:n], want1[:n])
+    assert layer.status.item() == 0
+
+
 def test_bounded_wait_times_out_and_the_context_survives(mx, cases):
     """A wait on a barrier nothing arrives at gives up after its limit with
     MOE_ERR_TIMEOUT on the status word; a second role leaves on the abort
