@@ -13,6 +13,8 @@
 //  2. rank: each block re-reads its chunk in (token, k) order, warp by warp,
 //     and gives each valid pair base + rank (a stable counting sort); the
 //     same blocks label m_indices by binary search over the segment starts.
+// When every pair fits in one chunk (a decode-sized batch), one block does
+// both passes in a single launch and no workspace is touched.
 #include <mutex>
 
 #include "common.cuh"
@@ -252,6 +254,124 @@ __global__ void __launch_bounds__(kThreads) layout_rank_kernel(
   }
 }
 
+// Small inputs (all pairs in one 2048-pair chunk, e.g. a decode batch): the
+// two passes above in one block and one launch. Count, scan over experts,
+// stable ranks and row labels, with the per-(expert, warp) counters in
+// dynamic shared memory (10 * E ints).
+__global__ void __launch_bounds__(kThreads) layout_single_kernel(
+    const int32_t* __restrict__ ids, int64_t T, int K, int E, int align,
+    const int32_t* __restrict__ d_n_valid, int64_t M_cap, int32_t* __restrict__ psum,
+    int32_t* __restrict__ start, int32_t* __restrict__ d_total, int32_t* __restrict__ tile_prefix,
+    int32_t* __restrict__ m_indices, int32_t* __restrict__ src2dst, int32_t* __restrict__ status) {
+  extern __shared__ int dyn[];
+  int* hist = dyn;                 // [E] counts
+  int* s_start = hist + E;         // [E]
+  int* wcnt = s_start + E;         // [kWarps][E]
+  __shared__ int warp_tot[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += kThreads) hist[e] = 0;
+  for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
+  __syncthreads();
+
+  const int64_t all_pairs = T * K;
+  const int64_t npairs = valid_rows(d_n_valid, T) * K;
+  // this warp's pairs in (token, k) order, loaded up front
+  const int64_t base_p = static_cast<int64_t>(warp) * kPairsPerWarp;
+  int idv[kRounds];
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j) {
+    const int64_t p = base_p + j * 32 + lane;
+    idv[j] = (p < npairs) ? ids[p] : -1;
+  }
+  int* my = wcnt + warp * E;
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j) {
+    const int id = idv[j];
+    if (id >= E) set_status(status, MOE_ERR_DEVICE_CHECK);
+    else if (id >= 0) {
+      atomicAdd(&hist[id], 1);
+      atomicAdd(&my[id], 1);
+    }
+  }
+  __syncthreads();
+
+  // Over experts: start = sum of aligned counts before, psum = start + count,
+  // the tile prefix and the total.
+  const int per = (E + kThreads - 1) / kThreads;
+  const int e0 = tid * per;
+  int rows_local = 0, tiles_local = 0;
+  for (int j = 0; j < per; ++j) {
+    const int e = e0 + j;
+    if (e < E) {
+      const int seg = align_up(hist[e], align);
+      rows_local += seg;
+      tiles_local += (seg + MOE_BLOCK_M - 1) / MOE_BLOCK_M;
+    }
+  }
+  int rows_total, tiles_total;
+  int run = block_exclusive_scan(rows_local, warp_tot, &rows_total);
+  int trun = block_exclusive_scan(tiles_local, warp_tot, &tiles_total);
+  for (int j = 0; j < per; ++j) {
+    const int e = e0 + j;
+    if (e < E) {
+      const int c = hist[e];
+      const int seg = align_up(c, align);
+      start[e] = run;
+      s_start[e] = run;
+      psum[e] = run + c;
+      tile_prefix[e] = trun;
+      run += seg;
+      trun += (seg + MOE_BLOCK_M - 1) / MOE_BLOCK_M;
+    }
+  }
+  if (tid == 0) {
+    tile_prefix[E] = tiles_total;
+    *d_total = rows_total;
+    if (rows_total > M_cap) set_status(status, MOE_ERR_DEVICE_CHECK);
+  }
+  __syncthreads();
+  // per expert, each warp's first row: the segment start plus the earlier
+  // warps' pairs of that expert
+  for (int e = tid; e < E; e += kThreads) {
+    int acc = s_start[e];
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  // stable ranks, 32 pairs at a time (lanes with the same expert ranked by lane)
+  const unsigned lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j) {
+    const int64_t p = base_p + j * 32 + lane;
+    const int id = idv[j];
+    const bool valid = (id >= 0 && id < E);
+    const int key = valid ? id : (E + static_cast<int>(lane));
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    int dst = -1;
+    if (valid) dst = my[id] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (valid && (peers & lt_mask) == 0u) my[id] += __popc(peers);
+    __syncwarp();
+    if (p < all_pairs) src2dst[p] = (dst >= 0 && dst < M_cap) ? dst : -1;
+  }
+  // row labels
+  for (int64_t row = tid; row < M_cap; row += kThreads) {
+    int label = -1;
+    if (row < rows_total) {
+      int lo = 0, hi = E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_start[mid] <= row) lo = mid; else hi = mid - 1;
+      }
+      label = lo;
+    }
+    m_indices[row] = label;
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -285,6 +405,14 @@ extern "C" int moe_expand_layout(const int32_t* topk_ids, int64_t T, int K, int 
   int32_t* offs = counts + static_cast<int64_t>(E) * nb;
   unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + need - 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (nb == 1) {
+    // every pair in one chunk: one block, one launch, no workspace
+    const size_t smem = static_cast<size_t>(moe::kWarps + 2) * E * sizeof(int);
+    moe::layout_single_kernel<<<1, moe::kThreads, smem, s>>>(topk_ids, T, K, E, align, d_n_valid,
+                                                            M_cap, psum, start, d_total, tile_prefix,
+                                                            m_indices, src2dst, d_status);
+    return moe::check_launch("layout_single_kernel");
+  }
   moe::layout_count_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, align, d_n_valid, M_cap,
                                                         nb, counts, offs, ticket, psum, start,
                                                         d_total, tile_prefix, d_status);
