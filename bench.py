@@ -33,7 +33,7 @@ import torch  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "MoE prefill layer tokens/s; scatter+combine HBM GB/s; grouped FP8 TFLOP/s"
-WORKLOAD = synth.CONFIGS[2]          # zipf_t16384_h7168
+WORKLOAD = synth.config_by_name("zipf_t16384_h7168")
 L2_FLUSH_BYTES = 256 << 20           # > the 126 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_PER_BF16 = 2.0                   # nominal dense fp8 : bf16 tensor rate

@@ -100,7 +100,7 @@ EXTRA_CONFIGS = (
 # Shapes small enough for the oracle to run every row in seconds, still
 # spanning several 128-row tiles, several N tiles and ragged tails.
 PARITY_CONFIGS = (
-    CONFIGS[0],
+    next(c for c in CONFIGS if c.name == "tiny_h512"),
     LayerConfig("mid_f32", T=200, H=1024, I=512, E=8, K=4, align=128, seed=10,
                 routing="uniform", inactive_frac=0.10),
     LayerConfig("mid_ue8m0", T=192, H=1024, I=512, E=8, K=4, align=128,

@@ -27,7 +27,7 @@ def _worker(rank, world, port, q):
     step_ms = 10.0 + 5.0 * r            # rank 1 is the slow one
     mx = bench.reduce_max(step_ms, w, "cpu")
     tok = bench.reduce_sum(1000.0 + r, w, "cpu")
-    cfg = bench.rank_config(synth.CONFIGS[1], r)
+    cfg = bench.rank_config(synth.config_by_name("uniform_t4096_h4096"), r)
     bench.barrier(w)
     q.put((r, mx, tok, cfg.seed))
     torch.distributed.destroy_process_group()
@@ -51,7 +51,7 @@ def test_two_gloo_ranks_aggregate():
 
 def test_algorithmic_work_counts():
     import bench
-    cfg = synth.CONFIGS[2]
+    cfg = synth.config_by_name("zipf_t16384_h7168")
     w = bench.algorithmic_work(cfg, P=1000, M_pad=1280, nv=130)
     H, I = cfg.H, cfg.I
     assert w["gemm1"] == 2.0 * 1000 * 2 * I * H

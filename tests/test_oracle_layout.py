@@ -98,7 +98,7 @@ def _invariants(lay, ids, E, align, n_valid, M_cap):
         assert (np.diff(r) == 1).all() and (r.size == 0 or r[0] == start[e])
 
 
-@pytest.mark.parametrize("cfg", synth.PARITY_CONFIGS + synth.CONFIGS[1:3] + synth.CONFIGS[4:],
+@pytest.mark.parametrize("cfg", synth.PARITY_CONFIGS + tuple(synth.config_by_name(n) for n in ("uniform_t4096_h4096", "zipf_t16384_h7168", "padded_t32768_valid6000_h4096")),
                          ids=lambda c: c.name)
 def test_layout_invariants_on_workloads(orc, cfg):
     d = synth.generate(cfg, with_weights=False)
