@@ -62,6 +62,26 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same test, but a thread whose phase is not complete yet may sleep in it for
+// up to `ns` nanoseconds; it wakes as soon as the phase completes. Spinning
+// on the plain form returns every few tens of cycles and takes issue slots
+// from the other warps of the same scheduler.
+MOE_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Longest sleep of one test inside a bounded wait: short against the wait
+// limit, so the abort flag and the limit are still checked often.
+constexpr uint32_t kWaitSleepNs = 20000;
+
 // Waits until the phase with the given parity has completed. Gives up when
 // *abort becomes non-zero (another role gave up) or after kWaitLimitCycles,
 // in which case it records MOE_ERR_TIMEOUT, raises *abort and returns false.
@@ -70,9 +90,27 @@ MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int3
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*abort) return false;
     if (clock64() - t0 > limit_cycles) {
+      *abort = 1;
+      set_status(status, MOE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Warp-collective form of mbar_wait: every lane of the warp calls it and all
+// lanes leave together, so the loop stays warp-uniform (no per-lane exits to
+// reconverge, no separate vote afterwards).
+MOE_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status,
+                            long long limit_cycles = kWaitLimitCycles) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kWaitSleepNs))) return true;
+    if (__any_sync(0xffffffffu, *abort != 0)) return false;
+    if (__any_sync(0xffffffffu, clock64() - t0 > limit_cycles)) {
       *abort = 1;
       set_status(status, MOE_ERR_TIMEOUT);
       return false;

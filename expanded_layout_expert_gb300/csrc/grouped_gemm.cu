@@ -13,7 +13,8 @@
 //  - warp 0, one lane: TMA producer. Per 128-wide K block it loads the
 //    128-row A tile and the BN-row W tile (128-byte swizzle) into a ring of
 //    shared-memory stages.
-//  - warp 1, one lane: tcgen05.mma issuer (kind::f8f6f4, M=128, N=BN, K=32,
+//  - warps 1 and 2, one lane each: tcgen05.mma issuers for the even and the
+//    odd K blocks (kind::f8f6f4, M=128, N=BN, K=32,
 //    4 instructions per K block). Each K block is accumulated into a fresh
 //    TMEM buffer (512/BN of them in a ring), because the fp32 block scales
 //    cannot be applied inside the tensor core.
@@ -22,7 +23,7 @@
 //    partial sums with tcgen05.ld, 64 columns per wait, frees the TMEM buffer
 //    as soon as its last read has landed, and adds sA * sW * partial into
 //    fp32 registers with packed fma.rn.f32x2 ("promotion").
-//  - warps 2-3 are spare; with BN = 256 warpgroup 0 hands its registers to
+//  - warp 3 is spare; with BN = 256 warpgroup 0 hands its registers to
 //    the epilogue warpgroups (setmaxnreg). Scale words are loaded two
 //    K blocks before use and decoded only then, so no global load is waited
 //    for early. At the end of the tile it converts to bf16 and stores its row
@@ -131,7 +132,7 @@ struct Params {
 // Bounded wait used while draining: no abort check, only the time limit.
 MOE_DEV void drain_wait(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) {
     if (clock64() - t0 > kWaitLimitCycles) return;
   }
 }
@@ -145,8 +146,8 @@ MOE_DEV uint32_t pack_bf16x2(float a, float b) {
 enum TraceSlot {
   kTrKernel = 0,      // whole kernel (thread 0)
   kTrProdWait = 1,    // producer waiting for a free stage
-  kTrMmaWaitTmem = 2, // MMA waiting for a free TMEM buffer
-  kTrMmaWaitData = 3, // MMA waiting for TMA data
+  kTrMmaWaitTmem = 2, // MMA issuers waiting for a free TMEM buffer (summed)
+  kTrMmaWaitData = 3, // MMA issuers waiting for TMA data (summed)
   kTrEpiWait = 4,     // epilogue warp 4: waiting for a full accumulator
   kTrEpiTile = 5,     // epilogue warp 4: tile-end work (store, or act+quant)
   kTrUnused6 = 6,
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], C::kEpiWarps);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, 2);  // one commit per MMA issuer
     if (Fused)
       for (int q = 0; q < 4; ++q) mbar_init(&amax_bar[q], 64);  // both warps of the quarter
     *abort_flag = 0;
@@ -291,15 +292,27 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
         if (s < 0) { s += C::kStages; ph ^= 1u; }
         drain_wait(&full[s], ph);
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if ((warp == 1 || warp == 2) && lane == 0) {
+      // ---------------------------------------------------------- MMA issuers
+      // Two threads issue the MMAs: warp 1 the even K blocks of the CTA's
+      // running count, warp 2 the odd ones, each with its own accumulator
+      // buffer when there are two. An MMA issue blocks while the tensor
+      // pipe's queue is full, so with one thread the pipe drains while that
+      // thread waits on its two barriers; with two, one waits while the
+      // other issues. K blocks are independent (own accumulator, own stage),
+      // so the order in which the pipe takes them changes no result.
       constexpr uint32_t idesc = idesc_f8_f32(BM, BN);
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      const int par = warp - 1;
       unsigned long long t_tmem = 0, t_data = 0, nkb = 0;
-      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-        bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
+      long long g = 0;  // the CTA's running K-block count
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          if (static_cast<int>(g & 1) != par) continue;
+          const int stage = static_cast<int>(g % C::kStages);
+          const uint32_t phase = static_cast<uint32_t>((g / C::kStages) & 1);
+          const int acc = static_cast<int>(g % C::kAcc);
+          const uint32_t acc_phase = static_cast<uint32_t>((g / C::kAcc) & 1);
           const long long t0 = tracing ? clock64() : 0;
           if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           const long long t1 = tracing ? clock64() : 0;
@@ -320,17 +333,15 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
                       idesc, k > 0 ? 1u : 0u);
           tc_commit(&empty[stage]);
           tc_commit(&tfull[acc]);
-          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-          if (++acc == C::kAcc) { acc = 0; acc_phase ^= 1u; }
         }
-        if (!ok) break;
       }
-      if (tracing) {
-        s_trace[kTrMmaWaitTmem] = t_tmem;
-        s_trace[kTrMmaWaitData] = t_data;
-        s_trace[kTrKBlocks] = nkb;
+      if (tracing) {  // summed over both issuers
+        atomicAdd(&s_trace[kTrMmaWaitTmem], t_tmem);
+        atomicAdd(&s_trace[kTrMmaWaitData], t_data);
+        atomicAdd(&s_trace[kTrKBlocks], nkb);
       }
-      // Every MMA issued so far must complete before TMEM is released.
+      // Every MMA issued so far must complete before TMEM is released
+      // (mma_done counts one arrival per issuer).
       tc_commit(mma_done);
       drain_wait(mma_done, 0);
     }
@@ -396,14 +407,11 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
       // soon as the last read has landed.
       auto kblock = [&](int kb, uint32_t& ra, uint32_t& rw, uint32_t& rw1) {
         if (!ok || kb >= KB) return;
-        const float sc0 = decode(kb, ra, rw);
-        const float sc1 = Fused ? decode(kb, ra, rw1) : sc0;
-        load_raw(kb + 2, ra, rw, rw1);
         // all lanes leave together: the TMEM loads below are warp-collective
         const long long tw0 = tracing ? clock64() : 0;
-        const bool got = mbar_wait(&tfull[acc_buf], acc_phase, abort_flag, p.status);
+        const bool got = mbar_wait_warp(&tfull[acc_buf], acc_phase, abort_flag, p.status);
         if (tracing) t_epi_wait += clock64() - tw0;
-        if (!__all_sync(0xffffffffu, got)) {
+        if (!got) {
           ok = false;
           return;
         }
@@ -414,14 +422,22 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
         // read, before that batch is promoted, so the MMA can reuse it as
         // early as possible.
         constexpr int kBatches = C::kColsPerWarp / 64;
+        float sc0 = 0.0f, sc1 = 0.0f;
 #pragma unroll
         for (int bt = 0; bt < kBatches; ++bt) {
           const uint32_t bcol = Fused ? static_cast<uint32_t>(bt * 128 + half * 64)
                                       : static_cast<uint32_t>(half * C::kColsPerWarp + bt * 64);
-          const float2 sc = bt == 0 ? make_float2(sc0, sc0) : make_float2(sc1, sc1);
           uint32_t va[32], vb[32];
           tc_ld32(tq + bcol, va);
           tc_ld32(tq + bcol + 32, vb);
+          if (bt == 0) {
+            // decode this K block's scales and fetch those of K block kb + 2
+            // while the first TMEM load is in flight
+            sc0 = decode(kb, ra, rw);
+            sc1 = Fused ? decode(kb, ra, rw1) : sc0;
+            load_raw(kb + 2, ra, rw, rw1);
+          }
+          const float2 sc = bt == 0 ? make_float2(sc0, sc0) : make_float2(sc1, sc1);
           tc_wait64(va, vb);
           if (bt == kBatches - 1) {
             tc_fence_before();
@@ -468,9 +484,9 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
         const int par = iter & 1;
         s_amax[(par * 2 + half) * 128 + row_in_tile] = m;
         mbar_arrive(&amax_bar[quarter]);
-        const bool got = mbar_wait(&amax_bar[quarter], static_cast<uint32_t>(par), abort_flag,
-                                   p.status);
-        if (!__all_sync(0xffffffffu, got)) break;
+        const bool got = mbar_wait_warp(&amax_bar[quarter], static_cast<uint32_t>(par),
+                                        abort_flag, p.status);
+        if (!got) break;
         const float amax = fmaxf(m, s_amax[(par * 2 + (half ^ 1)) * 128 + row_in_tile]);
         float sc, inv;
         uint32_t bexp;
@@ -850,8 +866,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
         const float sc1 = decode(kb, ra, rw);
         const float2 sc = make_float2(sc1, sc1);
         load_raw(kb + 2, ra, rw);
-        const bool got = mbar_wait(&tfull[acc_buf], acc_phase, abort_flag, p.status);
-        if (!__all_sync(0xffffffffu, got)) {
+        const bool got = mbar_wait_warp(&tfull[acc_buf], acc_phase, abort_flag, p.status);
+        if (!got) {
           ok = false;
           return;
         }

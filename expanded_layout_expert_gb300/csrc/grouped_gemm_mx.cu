@@ -104,7 +104,7 @@ constexpr int kTraceWords = 8;
 
 MOE_DEV void drain(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) {
     if (clock64() - t0 > kWaitLimitCycles) return;
   }
 }
@@ -321,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nbh1 = kFused ? I / 128 + tile % num_n : nbh0 + 1;
       bool ok = true;
       for (int g = 0; g < KG; ++g) {
-        const bool got = mbar_wait(&sf_empty[slot], sphase ^ 1u, abort_flag, p.status);
-        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        const bool got = mbar_wait_warp(&sf_empty[slot], sphase ^ 1u, abort_flag, p.status);
+        if (!got) { ok = false; break; }
         uint32_t a[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row_in_tile = quarter * 32 + lane;
       const int row = row0 + row_in_tile;
       const bool row_ok = row_in_tile < rows && row < p.M_cap;
-      const bool got = mbar_wait(tfull, acc_phase, abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, got)) break;
+      const bool got = mbar_wait_warp(tfull, acc_phase, abort_flag, p.status);
+      if (!got) break;
       const long long t1 = tracing ? clock64() : 0;
       tc_fence_after();
       const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
