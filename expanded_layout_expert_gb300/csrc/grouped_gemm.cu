@@ -148,7 +148,7 @@ enum TraceSlot {
   kTrProdWait = 1,    // producer waiting for a free stage
   kTrMmaWaitTmem = 2, // MMA issuers waiting for a free TMEM buffer (summed)
   kTrMmaWaitData = 3, // MMA issuers waiting for TMA data (summed)
-  kTrEpiWait = 4,     // epilogue warp 4: waiting for a full accumulator
+  kTrEpiWait = 4,     // unused (zero): timing the epilogue's waits slowed it
   kTrEpiTile = 5,     // epilogue warp 4: tile-end work (store, or act+quant)
   kTrUnused6 = 6,
   kTrKBlocks = 7,     // K blocks this CTA processed (count)
@@ -408,9 +408,7 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
       auto kblock = [&](int kb, uint32_t& ra, uint32_t& rw, uint32_t& rw1) {
         if (!ok || kb >= KB) return;
         // all lanes leave together: the TMEM loads below are warp-collective
-        const long long tw0 = tracing ? clock64() : 0;
         const bool got = mbar_wait_warp(&tfull[acc_buf], acc_phase, abort_flag, p.status);
-        if (tracing) t_epi_wait += clock64() - tw0;
         if (!got) {
           ok = false;
           return;

@@ -298,8 +298,8 @@ int moe_masked_slab_to_expand(const uint16_t* slab_out, int64_t max_m, const int
  * counters per CTA (grid = SM count) to d_trace: kernel cycles, producer
  * cycles waiting for a free stage, MMA cycles waiting for a free accumulator,
  * MMA cycles waiting for operand data, then (per-K-block promotion kernel)
- * epilogue cycles waiting for an accumulator, epilogue cycles in tile-end
- * work, one unused word, or (block-scaled kernel) MMA cycles waiting for
+ * one unused word, epilogue cycles in tile-end work, one unused word, or
+ * (block-scaled kernel) MMA cycles waiting for
  * scales, epilogue wait, epilogue tile work; last, K blocks processed. NULL
  * turns it off. Not thread-safe with respect to concurrent launches on other
  * threads. */
