@@ -164,7 +164,12 @@ enum TraceSlot {
 // forms h = bf16(silu(bf16 g) * bf16 u), exchanges its row maximum with the
 // other warp of its lane quarter, and writes codes and the group's scale.
 // The arithmetic is that of the stand-alone launches, bit for bit.
-template <int BN, bool Staged, bool Fused>
+//
+// Ue8m0 fixes the scale format at compile time (p.ue8m0 says the same at run
+// time): the per-K-block scale loads and decode are in the epilogue's inner
+// loop, and selecting between the two formats there cost 5-9 % of the
+// kernel's time.
+template <int BN, bool Staged, bool Fused, bool Ue8m0>
 __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const Params p) {
@@ -384,16 +389,16 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
           rw1 = 0u;
           return;
         }
-        rw = p.ue8m0 ? static_cast<uint32_t>(ws8[wbase + kb]) : __float_as_uint(wsf[wbase + kb]);
+        rw = Ue8m0 ? static_cast<uint32_t>(ws8[wbase + kb]) : __float_as_uint(wsf[wbase + kb]);
         if (Fused)
-          rw1 = p.ue8m0 ? static_cast<uint32_t>(ws8[wbase1 + kb]) : __float_as_uint(wsf[wbase1 + kb]);
+          rw1 = Ue8m0 ? static_cast<uint32_t>(ws8[wbase1 + kb]) : __float_as_uint(wsf[wbase1 + kb]);
         ra = 0u;
         if (row_ok)
-          ra = p.ue8m0 ? asw[static_cast<int64_t>(kb >> 2) * p.ld_as + row]
+          ra = Ue8m0 ? asw[static_cast<int64_t>(kb >> 2) * p.ld_as + row]
                        : __float_as_uint(asf[static_cast<int64_t>(row) * p.ld_as + kb]);
       };
       auto decode = [&](int kb, uint32_t ra, uint32_t rw) -> float {
-        if (p.ue8m0) return ue8m0_to_f32((ra >> (8 * (kb & 3))) & 0xFFu) * ue8m0_to_f32(rw);
+        if (Ue8m0) return ue8m0_to_f32((ra >> (8 * (kb & 3))) & 0xFFu) * ue8m0_to_f32(rw);
         return __uint_as_float(ra) * __uint_as_float(rw);
       };
 
@@ -488,7 +493,7 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
         const float amax = fmaxf(m, s_amax[(par * 2 + (half ^ 1)) * 128 + row_in_tile]);
         float sc, inv;
         uint32_t bexp;
-        group_scale(amax, p.ue8m0 != 0, sc, inv, bexp);
+        group_scale(amax, Ue8m0, sc, inv, bexp);
         if (row_ok) {
           uint8_t* di = reinterpret_cast<uint8_t*>(p.out);
           uint4* dst = reinterpret_cast<uint4*>(di + static_cast<int64_t>(row) * I +
@@ -505,7 +510,7 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
             dst[q] = make_uint4(lo.x, lo.y, hi.x, hi.y);
           }
           if (half == 0) {
-            if (p.ue8m0) {
+            if (Ue8m0) {
               // byte t%4 of word (t/4, row); the last group also clears the
               // word's unused bytes
               uint8_t* w = static_cast<uint8_t*>(p.di_scale) +
@@ -934,21 +939,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
 
 std::atomic<unsigned long long*> g_trace{nullptr};
 
-template <int BN, bool Staged, bool Fused = false>
-int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm, cudaStream_t s) {
+template <int BN, bool Staged, bool Fused, bool Ue8m0>
+int launch_fmt(const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm, cudaStream_t s) {
   using C = Cfg<BN, Staged, Fused>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<BN, Staged, Fused>,
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<BN, Staged, Fused, Ue8m0>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
       return check_launch("cudaFuncSetAttribute(grouped_gemm_kernel)");
     attr_set[dev] = true;
   }
-  grouped_gemm_kernel<BN, Staged, Fused><<<device_sm_count(), C::kThreads, C::kSmemBytes, s>>>(
-      ta, tb, prm);
+  grouped_gemm_kernel<BN, Staged, Fused, Ue8m0>
+      <<<device_sm_count(), C::kThreads, C::kSmemBytes, s>>>(ta, tb, prm);
   return check_launch("grouped_gemm_kernel");
+}
+
+template <int BN, bool Staged, bool Fused = false>
+int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm, cudaStream_t s) {
+  return prm.ue8m0 ? launch_fmt<BN, Staged, Fused, true>(ta, tb, prm, s)
+                   : launch_fmt<BN, Staged, Fused, false>(ta, tb, prm, s);
 }
 
 int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm, cudaStream_t s) {
