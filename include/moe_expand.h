@@ -306,11 +306,15 @@ int moe_masked_slab_to_expand(const uint16_t* slab_out, int64_t max_m, const int
 int moe_gemm_set_trace(uint64_t* d_trace);
 
 /* Diagnostics (no counterpart in the pages): runs the library's bounded
- * mbarrier wait on a barrier nothing arrives at. One waiter gives up after
- * limit_cycles (0 < limit <= 4e9; the kernels use ~4e9), writes
- * MOE_ERR_TIMEOUT to *d_status and raises its block's abort flag; a second
- * waiter with a 4x longer limit leaves on the flag. d_out (device int64 [4]):
- * first waiter's result (0 = gave up) and cycles waited, then the second's. */
+ * mbarrier waits on barriers nothing arrives at. Block 0: a single-thread
+ * waiter gives up after limit_cycles (0 < limit <= 4e9; the kernels use
+ * ~4e9), writes MOE_ERR_TIMEOUT to *d_status and raises its block's abort
+ * flag; a second single-thread waiter and a warp in the warp-collective wait,
+ * each with a 4x longer limit, leave on the flag. Block 1: a warp in the
+ * warp-collective wait gives up on its own limit. d_out (device int64 [8]):
+ * per waiter its result (single thread: 1 = phase completed, 0 = gave up;
+ * warp: the ballot of lanes that saw completion) and the cycles it waited,
+ * in that order. */
 int moe_selftest_bounded_wait(int64_t limit_cycles, int32_t* d_status, int64_t* d_out,
                               moe_stream_t stream);
 

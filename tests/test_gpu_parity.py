@@ -396,10 +396,12 @@ def test_captured_forward_replays(mx, cases, mode):
 
 def test_bounded_wait_times_out_and_the_context_survives(mx, cases):
     """A wait on a barrier nothing arrives at gives up after its limit with
-    MOE_ERR_TIMEOUT on the status word; a second role leaves on the abort
-    flag well before its own (longer) limit; the device keeps working."""
+    MOE_ERR_TIMEOUT on the status word; the other roles (a single thread and
+    a warp in the warp-collective wait) leave on the abort flag well before
+    their own (longer) limit; a warp-collective waiter alone gives up on its
+    own limit, all lanes together; the device keeps working."""
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = torch.full((4,), -1, dtype=torch.int64, device="cuda")
+    out = torch.full((8,), -1, dtype=torch.int64, device="cuda")
     limit = 2_000_000  # about 1 ms
     mx.check(mx.load().moe_selftest_bounded_wait(limit, status.data_ptr(), out.data_ptr(),
                                                   torch.cuda.current_stream().cuda_stream),
@@ -409,6 +411,8 @@ def test_bounded_wait_times_out_and_the_context_survives(mx, cases):
     assert status.item() == mx._capi.MOE_ERR_TIMEOUT
     assert o[0] == 0 and o[1] >= limit
     assert o[2] == 0 and o[3] < 4 * limit, "the second waiter left on the abort flag"
+    assert o[4] == 0 and o[5] < 4 * limit, "the waiting warp left on the abort flag"
+    assert o[6] == 0 and o[7] >= limit, "a waiting warp gives up on its own limit"
     # the context is still usable: a whole layer runs and matches the oracle
     c = cases["tiny_h512"]
     g = c["g"]
