@@ -66,6 +66,9 @@ def parse_args(argv=None):
                     help="decode variant: both GEMMs on per-expert slabs of this height")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of a CUDA graph of the whole forward (no per-kernel split)")
+    ap.add_argument("--fuse-layout-scatter", action="store_true",
+                    help="layout and expand-scatter as one call of two launches "
+                         "(moe_expand_layout_scatter)")
     ap.add_argument("--unfused", action="store_true",
                     help="run gate_up and act+quant as two launches")
     ap.add_argument("--gemm-tile-n128", action="store_true",
@@ -198,6 +201,16 @@ def algorithmic_work(cfg, P: int, M_pad: int, nv: int):
 
 # ------------------------------------------------------------------ our arm
 
+def launches_per_step(args, cfg, fused: bool) -> int:
+    """Kernels one step launches: layout 2 (1 when all pairs fit one
+    2048-pair chunk) + scatter 1, or 2 for the fused layout+scatter call;
+    gate_up (with act+quant when fused, else + act_quant 1); down 1 (the
+    masked slab adds its two bridges); combine 1."""
+    one_chunk = cfg.T * cfg.K <= 2048
+    front = 2 if args.fuse_layout_scatter else (2 if one_chunk else 3)
+    ffn = 4 if args.masked_max_m else (2 if fused else 3)
+    return front + ffn + 1
+
 def run_ours(args, world, rank, local):
     import expanded_layout_expert_gb300 as mx
     from expanded_layout_expert_gb300 import build as libbuild
@@ -212,7 +225,8 @@ def run_ours(args, world, rank, local):
     n_valid = torch.tensor([nv], dtype=torch.int32, device=dev)
     layer = mx.ExpandedMoELayer(d["w13"], d["s13"], d["w2"], d["s2"], K=cfg.K, align=cfg.align,
                                 scale_mode=cfg.scale_mode, max_tokens=cfg.T, weighting=args.weighting,
-                                masked_max_m=args.masked_max_m or None)
+                                masked_max_m=args.masked_max_m or None,
+                                fuse_layout_scatter=args.fuse_layout_scatter)
     L = mx.load()
     stream = torch.cuda.current_stream()
     s = stream.cuda_stream
@@ -232,17 +246,30 @@ def run_ours(args, world, rank, local):
             if ev is not None:
                 ev[i].record(stream)
         mark(0)
-        mx.check(L.moe_expand_layout(ptr(ids), cfg.T, cfg.K, cfg.E, cfg.align, ptr(n_valid),
-                                     layer.M_cap, ptr(lay.psum), ptr(lay.start), ptr(lay.total),
-                                     ptr(lay.m_indices), ptr(lay.src2dst), ptr(lay.tile_prefix),
-                                     ptr(layer.ws), layer.ws.numel(), ptr(layer.status), s), "layout")
-        mark(1)
-        mx.check(L.moe_expand_scatter(ptr(x_q), ptr(x_s), layer.sl, x_s.shape[1], ptr(w),
-                                      ptr(lay.src2dst), ptr(lay.psum), ptr(lay.start), ptr(n_valid),
-                                      cfg.T, cfg.H, cfg.K, cfg.E, cfg.align, layer.M_cap,
-                                      ptr(layer.xe), ptr(layer.xe_scale), layer.xe_scale.shape[1],
-                                      ptr(layer.row_w), ptr(layer.status), s), "scatter")
-        mark(2)
+        if args.fuse_layout_scatter:
+            # both in one call: its time is booked to "scatter"
+            mark(1)
+            mx.check(L.moe_expand_layout_scatter(
+                ptr(ids), ptr(w), ptr(x_q), ptr(x_s), layer.sl, x_s.shape[1], cfg.T, cfg.H, cfg.K,
+                cfg.E, cfg.align, ptr(n_valid), layer.M_cap, ptr(lay.psum), ptr(lay.start),
+                ptr(lay.total), ptr(lay.m_indices), ptr(lay.src2dst), ptr(lay.tile_prefix),
+                ptr(layer.xe), ptr(layer.xe_scale), layer.xe_scale.shape[1], ptr(layer.row_w),
+                ptr(layer.ws), layer.ws.numel(), ptr(layer.status), s), "layout+scatter")
+            mark(2)
+        else:
+            mx.check(L.moe_expand_layout(ptr(ids), cfg.T, cfg.K, cfg.E, cfg.align, ptr(n_valid),
+                                         layer.M_cap, ptr(lay.psum), ptr(lay.start), ptr(lay.total),
+                                         ptr(lay.m_indices), ptr(lay.src2dst), ptr(lay.tile_prefix),
+                                         ptr(layer.ws), layer.ws.numel(), ptr(layer.status), s),
+                     "layout")
+            mark(1)
+            mx.check(L.moe_expand_scatter(ptr(x_q), ptr(x_s), layer.sl, x_s.shape[1], ptr(w),
+                                          ptr(lay.src2dst), ptr(lay.psum), ptr(lay.start),
+                                          ptr(n_valid), cfg.T, cfg.H, cfg.K, cfg.E, cfg.align,
+                                          layer.M_cap, ptr(layer.xe), ptr(layer.xe_scale),
+                                          layer.xe_scale.shape[1], ptr(layer.row_w),
+                                          ptr(layer.status), s), "scatter")
+            mark(2)
         if layer.masked_max_m is not None:
             # decode variant: slab in, fused gate_up on the slab (segment
             # gemm1), down on the slab and back to expanded rows (gemm2)
@@ -369,6 +396,9 @@ def run_ours(args, world, rank, local):
         if fused and n == "act_quant":
             kernels[n] = {"ms": 0.0, "fused_into": "gemm1"}
             continue
+        if args.fuse_layout_scatter and n == "layout":
+            kernels[n] = {"ms": 0.0, "fused_into": "scatter"}
+            continue
         if n.startswith("gemm"):
             ach = work[n] / (ms / 1e3) / 1e12
             kernels[n] = {"ms": round(ms, 4), "achieved": round(ach, 1), "unit": "TFLOP/s",
@@ -405,6 +435,7 @@ def run_ours(args, world, rank, local):
                    "weighting": args.weighting,
                    "masked_max_m": args.masked_max_m or None,
                    "cuda_graph": bool(args.graph),
+                   "layout_scatter": "one call, 2 launches" if args.fuse_layout_scatter else "2 calls",
                    "valid_pairs": P, "expanded_rows": M_pad, "M_cap": layer.M_cap,
                    "l2": "flushed between steps (256 MiB write outside the timed events)",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
@@ -412,7 +443,7 @@ def run_ours(args, world, rank, local):
         "grouped_fp8_tflops": None if args.graph else round(gemm_tflops, 1),
         "kernels": kernels,
         "roofline": roofline,
-        "gpu_launches": (8 if args.masked_max_m else (6 if fused else 7)) * args.steps,
+        "gpu_launches": launches_per_step(args, cfg, fused) * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": round(t_wall, 3),
     }

@@ -21,7 +21,8 @@ from ._capi import (MOE_BLOCK_M, MOE_FFN_UNFUSED, MOE_FOLD_WEIGHT_INTO_SCALE, MO
                     MOE_WEIGHT_OUTPUT_ROWS, MoEError, check, load)
 
 __all__ = [
-    "expanded_capacity", "workspace_size", "expand_layout", "expand_scatter", "grouped_gemm",
+    "expanded_capacity", "workspace_size", "expand_layout", "expand_scatter",
+    "expand_layout_scatter", "grouped_gemm",
     "act_quant", "grouped_gemm_act_quant", "grouped_ffn", "combine", "ExpandedMoELayer",
     "HostPipeline", "CapturedForward", "Layout",
     "MoEError",
@@ -125,6 +126,44 @@ def expand_scatter(x_q: torch.Tensor, x_scale: torch.Tensor, scale_layout: int,
                                    _ptr(row_w), _ptr(status), _stream(stream))
     check(rc, "moe_expand_scatter")
     return xe, xe_scale, row_w
+
+
+def expand_layout_scatter(x_q: torch.Tensor, x_scale: torch.Tensor, scale_layout: int,
+                          topk_ids: torch.Tensor, topk_w: torch.Tensor, E: int, align: int,
+                          M_cap: int, n_valid: Optional[torch.Tensor] = None,
+                          ws: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                          out: Optional[Layout] = None, xe: Optional[torch.Tensor] = None,
+                          xe_scale: Optional[torch.Tensor] = None,
+                          row_w: Optional[torch.Tensor] = None, stream=None):
+    """The layout and the expand-scatter in two launches (the layout's
+    count/scan, then rank + copy per chunk); same outputs as expand_layout
+    followed by expand_scatter. Returns (layout, xe, xe_scale, row_w)."""
+    T, H = x_q.shape
+    K = topk_ids.shape[1]
+    dev = x_q.device
+    if out is None:
+        out = Layout(psum=torch.empty(E, dtype=torch.int32, device=dev),
+                     start=torch.empty(E, dtype=torch.int32, device=dev),
+                     total=torch.empty(1, dtype=torch.int32, device=dev),
+                     m_indices=torch.empty(M_cap, dtype=torch.int32, device=dev),
+                     src2dst=torch.empty(T, K, dtype=torch.int32, device=dev),
+                     tile_prefix=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                     E=E, align=align, M_cap=M_cap)
+    if ws is None:
+        ws = torch.zeros(workspace_size(T, K, E), dtype=torch.uint8, device=dev)
+    if xe is None:
+        xe = torch.zeros(M_cap, H, dtype=torch.uint8, device=dev)
+    if xe_scale is None:
+        xe_scale = new_scale(M_cap, H // 128, scale_layout, dev)
+    if row_w is None:
+        row_w = torch.zeros(M_cap, dtype=torch.float32, device=dev)
+    rc = load().moe_expand_layout_scatter(
+        _ptr(topk_ids), _ptr(topk_w), _ptr(x_q), _ptr(x_scale), scale_layout, x_scale.shape[1], T,
+        H, K, E, align, _ptr(n_valid), M_cap, _ptr(out.psum), _ptr(out.start), _ptr(out.total),
+        _ptr(out.m_indices), _ptr(out.src2dst), _ptr(out.tile_prefix), _ptr(xe), _ptr(xe_scale),
+        xe_scale.shape[1], _ptr(row_w), _ptr(ws), ws.numel(), _ptr(status), _stream(stream))
+    check(rc, "moe_expand_layout_scatter")
+    return out, xe, xe_scale, row_w
 
 
 def grouped_gemm(A: torch.Tensor, A_scale: torch.Tensor, scale_layout: int, lay: Layout,
@@ -238,11 +277,15 @@ class ExpandedMoELayer:
     / moe_masked_slab_to_expand); the weight multiplies each pair's down row
     on the way back (no fold); an expert with more rows than masked_max_m
     drops the extra ones and flags the status word.
+    fuse_layout_scatter: run the layout and the expand-scatter as
+    moe_expand_layout_scatter (two launches: count/scan, then rank + copy per
+    chunk) instead of moe_expand_layout + moe_expand_scatter (three); the
+    outputs are the same bit for bit.
     """
 
     def __init__(self, w13, s13, w2, s2, *, K: int, align: int, scale_mode: str,
                  max_tokens: int, device=None, weighting: str = "expanded",
-                 masked_max_m: Optional[int] = None):
+                 masked_max_m: Optional[int] = None, fuse_layout_scatter: bool = False):
         self.w13, self.s13, self.w2, self.s2 = w13, s13, w2, s2
         self.E, twoI, self.H = w13.shape
         self.I = twoI // 2
@@ -255,6 +298,7 @@ class ExpandedMoELayer:
             raise ValueError("the masked-slab path weights rows after the slab; use the default weighting")
         self.weighting = weighting
         self.masked_max_m = masked_max_m
+        self.fuse_layout_scatter = bool(fuse_layout_scatter)
         if weighting == "gather" or masked_max_m is not None:
             self.flags = 0
         else:
@@ -310,17 +354,26 @@ class ExpandedMoELayer:
         L = load()
         s = _stream(stream)
         lay = self.lay
-        check(L.moe_expand_layout(_ptr(topk_ids), T, self.K, self.E, self.align, _ptr(n_valid),
-                                  self.M_cap, _ptr(lay.psum), _ptr(lay.start), _ptr(lay.total),
-                                  _ptr(lay.m_indices), _ptr(lay.src2dst), _ptr(lay.tile_prefix),
-                                  _ptr(self.ws), self.ws.numel(), _ptr(self.status), s),
-              "moe_expand_layout")
-        check(L.moe_expand_scatter(_ptr(x_q), _ptr(x_scale), self.sl, x_scale.shape[1],
-                                   _ptr(topk_w), _ptr(lay.src2dst), _ptr(lay.psum),
-                                   _ptr(lay.start), _ptr(n_valid), T, self.H, self.K, self.E,
-                                   self.align, self.M_cap, _ptr(self.xe), _ptr(self.xe_scale),
-                                   self.xe_scale.shape[1], _ptr(self.row_w), _ptr(self.status),
-                                   s), "moe_expand_scatter")
+        if self.fuse_layout_scatter:
+            check(L.moe_expand_layout_scatter(
+                _ptr(topk_ids), _ptr(topk_w), _ptr(x_q), _ptr(x_scale), self.sl, x_scale.shape[1],
+                T, self.H, self.K, self.E, self.align, _ptr(n_valid), self.M_cap, _ptr(lay.psum),
+                _ptr(lay.start), _ptr(lay.total), _ptr(lay.m_indices), _ptr(lay.src2dst),
+                _ptr(lay.tile_prefix), _ptr(self.xe), _ptr(self.xe_scale), self.xe_scale.shape[1],
+                _ptr(self.row_w), _ptr(self.ws), self.ws.numel(), _ptr(self.status), s),
+                "moe_expand_layout_scatter")
+        else:
+            check(L.moe_expand_layout(_ptr(topk_ids), T, self.K, self.E, self.align,
+                                      _ptr(n_valid), self.M_cap, _ptr(lay.psum), _ptr(lay.start),
+                                      _ptr(lay.total), _ptr(lay.m_indices), _ptr(lay.src2dst),
+                                      _ptr(lay.tile_prefix), _ptr(self.ws), self.ws.numel(),
+                                      _ptr(self.status), s), "moe_expand_layout")
+            check(L.moe_expand_scatter(_ptr(x_q), _ptr(x_scale), self.sl, x_scale.shape[1],
+                                       _ptr(topk_w), _ptr(lay.src2dst), _ptr(lay.psum),
+                                       _ptr(lay.start), _ptr(n_valid), T, self.H, self.K, self.E,
+                                       self.align, self.M_cap, _ptr(self.xe), _ptr(self.xe_scale),
+                                       self.xe_scale.shape[1], _ptr(self.row_w),
+                                       _ptr(self.status), s), "moe_expand_scatter")
         if self.masked_max_m is not None:
             self._slab_ffn(L, s)
         else:
@@ -387,8 +440,9 @@ class ExpandedMoELayer:
                                        device=self.device)
         return self._gateup
 
-    # kernels one forward launches: layout 2, scatter 1, gate_up with
-    # act+quant fused 1, down 1, combine 1
+    # kernels one forward launches: layout 2 (1 when all pairs fit one
+    # 2048-pair chunk), scatter 1, gate_up with act+quant fused 1, down 1,
+    # combine 1; with fuse_layout_scatter, layout + scatter take 2
     KERNELS_PER_FORWARD = 6
 
 

@@ -48,6 +48,8 @@ SIGNATURES = {
     "moe_expand_layout": (I32, [P, I64, I32, I32, I32, P, I64, P, P, P, P, P, P, P, SZ, P, P]),
     "moe_expand_layout_noalloc": (I32, [P, I64, I32, I32, I32, P, I64, P, P, P, P, P, P, P, P]),
     "moe_expand_layout_noalloc_max_scratch": (SZ, []),
+    "moe_expand_layout_scatter": (I32, [P, P, P, P, I32, I64, I64, I32, I32, I32, I32, P, I64,
+                                        P, P, P, P, P, P, P, P, I64, P, P, SZ, P, P]),
     "moe_expand_scatter": (I32, [P, P, I32, I64, P, P, P, P, P, I64, I32, I32, I32, I32, I64,
                                  P, P, I64, P, P, P]),
     "moe_grouped_gemm": (I32, [P, P, I32, I64, P, P, P, P, P, P, I32, I32, I32, I32, I64, P, P, P]),

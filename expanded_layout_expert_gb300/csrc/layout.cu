@@ -518,3 +518,240 @@ extern "C" int moe_expand_layout_noalloc(const int32_t* topk_ids, int64_t T, int
                                                        offs, start, d_total, m_indices, src2dst);
   return moe::check_launch("layout_rank_kernel");
 }
+
+// ---------------------------------------------------------------------------
+// moe_expand_layout_scatter: the layout fused into the scatter (SGLang PR
+// 37261 names layout and scatter as the two light/heavy halves of the expand
+// step; here they share launches). Launch 1 is layout_count_kernel above
+// (per-chunk histograms, last-block scan). Launch 2 replaces both the rank
+// pass and the stand-alone scatter: S blocks per 2048-pair chunk each rank
+// the whole chunk exactly as layout_rank_kernel does (the ranks only need the
+// chunk's base rows from launch 1, and redoing them costs a few KB of id
+// reads), keep the destinations in shared memory and copy their share of the
+// chunk's tokens: each token's fp8 row and scale row read once and stored to
+// its destinations, with the pair's weight. The first of the S blocks writes
+// src2dst; blocks placed first in the grid zero the alignment gaps; the chunk
+// blocks label m_indices. The outputs are those of moe_expand_layout followed
+// by moe_expand_scatter, bit for bit.
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+constexpr int kPadRowsPerBlock = 8;
+
+__global__ void __launch_bounds__(kThreads) layout_rank_scatter_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ topk_w,
+    const uint4* __restrict__ x, const void* __restrict__ x_scale, int ue8m0, int64_t ld_xs,
+    int64_t T, int H, int K, int E, int align, const int32_t* __restrict__ d_n_valid,
+    int64_t M_cap, int nb, int S, const int32_t* __restrict__ offs,
+    const int32_t* __restrict__ psum, const int32_t* __restrict__ start,
+    const int32_t* __restrict__ d_total, int32_t* __restrict__ m_indices,
+    int32_t* __restrict__ src2dst, uint4* __restrict__ xe, void* __restrict__ xe_scale,
+    int64_t ld_xes, float* __restrict__ row_w, int pad_blocks_per_expert) {
+  __shared__ int wcnt[kWarps * kMaxE];
+  __shared__ int s_start[kMaxE];
+  __shared__ int s_dst[kChunk];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nvec = H / 16;
+  const int G = H / 128;
+  const int W = (G + 3) / 4;
+  const int pad_blocks = E * pad_blocks_per_expert;
+
+  if (static_cast<int>(blockIdx.x) < pad_blocks) {
+    // zero rows [psum[e], align(psum[e])) of expert e, 8 rows per block
+    const int e = blockIdx.x / pad_blocks_per_expert;
+    const int sub = blockIdx.x % pad_blocks_per_expert;
+    const int64_t seg_end = align_up(psum[e], align);
+    const int64_t r0 = static_cast<int64_t>(psum[e]) + static_cast<int64_t>(sub) * kPadRowsPerBlock;
+    int64_t r1 = r0 + kPadRowsPerBlock;
+    if (r1 > seg_end) r1 = seg_end;
+    if (r1 > M_cap) r1 = M_cap;
+    for (int64_t r = r0; r < r1; ++r) {
+      for (int v = tid; v < nvec; v += kThreads) xe[r * nvec + v] = make_uint4(0, 0, 0, 0);
+      if (!ue8m0) {
+        for (int g = tid; g < G; g += kThreads) static_cast<float*>(xe_scale)[r * ld_xes + g] = 0.0f;
+      } else {
+        for (int j = tid; j < W; j += kThreads) static_cast<int32_t*>(xe_scale)[j * ld_xes + r] = 0;
+      }
+      if (tid == 0) row_w[r] = 0.0f;
+    }
+    return;
+  }
+
+  const int cb = blockIdx.x - pad_blocks;  // chunk block
+  const int chunk = cb / S;
+  const int part = cb % S;
+  for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
+  for (int e = tid; e < E; e += kThreads) s_start[e] = start[e];
+  __syncthreads();
+
+  // --- ranks: the rank pass of layout_rank_kernel for this chunk
+  const int64_t all_pairs = T * K;
+  const int64_t npairs = valid_rows(d_n_valid, T) * K;
+  const int64_t p0 = static_cast<int64_t>(chunk) * kChunk;
+  const int64_t base_p = p0 + warp * kPairsPerWarp;
+  int* my = wcnt + warp * E;
+  int idv[kRounds];
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j) {
+    const int64_t p = base_p + j * 32 + lane;
+    idv[j] = (p < npairs) ? ids[p] : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j)
+    if (idv[j] >= 0 && idv[j] < E) atomicAdd(&my[idv[j]], 1);
+  __syncthreads();
+  for (int e = tid; e < E; e += kThreads) {
+    int acc = offs[static_cast<int64_t>(e) * nb + chunk];
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  const unsigned lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j) {
+    const int64_t p = base_p + j * 32 + lane;
+    const int id = idv[j];
+    const bool valid = (id >= 0 && id < E);
+    const int key = valid ? id : (E + static_cast<int>(lane));
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    int dst = -1;
+    if (valid) dst = my[id] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (valid && (peers & lt_mask) == 0u) my[id] += __popc(peers);
+    __syncwarp();
+    const int d = (dst >= 0 && dst < M_cap) ? dst : -1;
+    s_dst[warp * kPairsPerWarp + j * 32 + lane] = d;
+    if (part == 0 && p < all_pairs) src2dst[p] = d;
+  }
+  __syncthreads();
+
+  // --- copy: tokens of this chunk's valid pairs, every S-th one from `part`
+  int64_t p1 = p0 + kChunk;
+  if (p1 > npairs) p1 = npairs;
+  if (p1 > p0) {
+    const int64_t t_first = p0 / K;
+    const int64_t t_end = (p1 - 1) / K + 1;
+    for (int64_t t = t_first + part; t < t_end; t += S) {
+      const int64_t q0 = t * K;  // the token's first pair
+      const int k_lo = q0 < p0 ? static_cast<int>(p0 - q0) : 0;
+      const int k_hi = q0 + K > p1 ? static_cast<int>(p1 - q0) : K;
+      const int kb0 = static_cast<int>(q0 - p0);  // s_dst[kb0 + k]: pair k of token t
+      for (int v = tid; v < nvec; v += kThreads) {
+        const uint4 val = __ldcs(x + t * nvec + v);
+        for (int k = k_lo; k < k_hi; ++k) {
+          const int r = s_dst[kb0 + k];
+          if (r >= 0) xe[static_cast<int64_t>(r) * nvec + v] = val;
+        }
+      }
+      if (!ue8m0) {
+        const float* xs = static_cast<const float*>(x_scale);
+        for (int g = tid; g < G; g += kThreads) {
+          const float sv = xs[t * ld_xs + g];
+          for (int k = k_lo; k < k_hi; ++k) {
+            const int r = s_dst[kb0 + k];
+            if (r >= 0) static_cast<float*>(xe_scale)[static_cast<int64_t>(r) * ld_xes + g] = sv;
+          }
+        }
+      } else {
+        const int32_t* xs = static_cast<const int32_t*>(x_scale);
+        for (int j = tid; j < W; j += kThreads) {
+          const int32_t wv = xs[j * ld_xs + t];
+          for (int k = k_lo; k < k_hi; ++k) {
+            const int r = s_dst[kb0 + k];
+            if (r >= 0) static_cast<int32_t*>(xe_scale)[j * ld_xes + r] = wv;
+          }
+        }
+      }
+      if (tid >= k_lo && tid < k_hi && s_dst[kb0 + tid] >= 0) row_w[s_dst[kb0 + tid]] = topk_w[q0 + tid];
+    }
+  }
+
+  // --- row labels: e on [start[e], start[e] + align(count_e)), -1 past the total
+  const int total = *d_total;
+  const int64_t nchunk_blocks = static_cast<int64_t>(gridDim.x) - pad_blocks;
+  for (int64_t row = static_cast<int64_t>(cb) * kThreads + tid; row < M_cap;
+       row += nchunk_blocks * kThreads) {
+    int label = -1;
+    if (row < total) {
+      int lo = 0, hi = E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_start[mid] <= row) lo = mid; else hi = mid - 1;
+      }
+      label = lo;
+    }
+    m_indices[row] = label;
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_expand_layout_scatter(
+    const int32_t* topk_ids, const float* topk_w, const uint8_t* x, const void* x_scale,
+    int scale_layout, int64_t ld_xs, int64_t T, int H, int K, int E, int align,
+    const int32_t* d_n_valid, int64_t M_cap, int32_t* psum, int32_t* start, int32_t* d_total,
+    int32_t* m_indices, int32_t* src2dst, int32_t* tile_prefix, uint8_t* xe, void* xe_scale,
+    int64_t ld_xes, float* row_w, void* ws, size_t ws_bytes, int32_t* d_status,
+    moe_stream_t stream) {
+  MOE_REQUIRE(psum && start && d_total && tile_prefix && xe && xe_scale && row_w,
+              "moe_expand_layout_scatter: null output");
+  MOE_REQUIRE(T == 0 || (topk_ids && topk_w && x && x_scale && src2dst),
+              "moe_expand_layout_scatter: null input");
+  MOE_REQUIRE(M_cap == 0 || m_indices, "moe_expand_layout_scatter: null m_indices");
+  MOE_REQUIRE(T >= 0 && K > 0 && K <= 32 && E > 0 && E <= moe::kMaxE && align > 0 && M_cap >= 0,
+              "moe_expand_layout_scatter: bad sizes T=%lld K=%d E=%d align=%d M_cap=%lld",
+              (long long)T, K, E, align, (long long)M_cap);
+  MOE_REQUIRE(T * K <= INT32_MAX && M_cap <= INT32_MAX,
+              "moe_expand_layout_scatter: sizes exceed int32");
+  MOE_REQUIRE(H > 0 && H % 128 == 0 && H <= 16384,
+              "moe_expand_layout_scatter: H must be a multiple of 128, <= 16384");
+  MOE_REQUIRE(scale_layout == MOE_SCALE_F32_ROWMAJOR || scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR,
+              "moe_expand_layout_scatter: bad scale layout");
+  const int G = H / 128;
+  if (scale_layout == MOE_SCALE_F32_ROWMAJOR) {
+    MOE_REQUIRE(ld_xs >= G && ld_xes >= G,
+                "moe_expand_layout_scatter: scale leading dimension < H/128");
+  } else {
+    MOE_REQUIRE(ld_xs >= T && ld_xes >= M_cap,
+                "moe_expand_layout_scatter: packed scale leading dimension < rows");
+  }
+  MOE_REQUIRE(moe::aligned(x, 16) && moe::aligned(xe, 16),
+              "moe_expand_layout_scatter: x/xe not 16-byte aligned");
+  MOE_REQUIRE_DEVICE();
+  const size_t need = moe_workspace_size(T, K, E);
+  if (ws == nullptr || ws_bytes < need) {
+    moe::set_error("moe_expand_layout_scatter: workspace of %zu bytes needed", need);
+    return MOE_ERR_WORKSPACE;
+  }
+  const int nb = static_cast<int>(moe::num_chunks(T, K));
+  int32_t* counts = static_cast<int32_t*>(ws);
+  int32_t* offs = counts + static_cast<int64_t>(E) * nb;
+  unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + need - 256);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  moe::layout_count_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, align, d_n_valid, M_cap,
+                                                        nb, counts, offs, ticket, psum, start,
+                                                        d_total, tile_prefix, d_status);
+  int rc = moe::check_launch("layout_count_kernel");
+  if (rc != MOE_OK) return rc;
+  // S blocks per chunk: about four blocks per SM in all, and no more blocks
+  // per chunk than the chunk has tokens
+  int64_t tokens_per_chunk = (moe::kChunk + K - 1) / K + 1;
+  if (tokens_per_chunk > T + 1) tokens_per_chunk = T + 1;
+  int S = (4 * moe::device_sm_count() + nb - 1) / nb;
+  if (S > tokens_per_chunk) S = static_cast<int>(tokens_per_chunk);
+  if (S < 1) S = 1;
+  const int pad_per_expert = (align - 1 + moe::kPadRowsPerBlock - 1) / moe::kPadRowsPerBlock;
+  const int64_t grid = static_cast<int64_t>(E) * pad_per_expert + static_cast<int64_t>(nb) * S;
+  MOE_REQUIRE(grid < (1ll << 31), "moe_expand_layout_scatter: grid too large");
+  moe::layout_rank_scatter_kernel<<<static_cast<unsigned>(grid), moe::kThreads, 0, s>>>(
+      topk_ids, topk_w, reinterpret_cast<const uint4*>(x), x_scale,
+      scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR, ld_xs, T, H, K, E, align, d_n_valid, M_cap,
+      nb, S, offs, psum, start, d_total, m_indices, src2dst, reinterpret_cast<uint4*>(xe), xe_scale,
+      ld_xes, row_w, pad_per_expert);
+  return moe::check_launch("layout_rank_scatter_kernel");
+}

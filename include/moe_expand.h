@@ -141,6 +141,27 @@ int moe_expand_layout_noalloc(const int32_t* topk_ids, int64_t T, int K, int E, 
                               int32_t* m_indices, int32_t* src2dst, int32_t* tile_prefix,
                               int32_t* d_status, moe_stream_t stream);
 
+/*
+ * Layout fused into the expand-scatter (SGLang PR 37261: the layout kernels
+ * and the expand copy of the do_expand=True dispatch, here in two launches
+ * instead of three: the count/scan launch of moe_expand_layout, then one
+ * launch that ranks each 2048-pair chunk and copies that chunk's rows).
+ * Arguments: those of moe_expand_layout (topk_ids .. tile_prefix, the same
+ * workspace of moe_workspace_size bytes, zeroed before its first use) plus
+ * those of moe_expand_scatter (topk_w, x, x_scale/scale_layout/ld_xs, H, xe,
+ * xe_scale/ld_xes, row_w). Every output equals, bit for bit, what
+ * moe_expand_layout followed by moe_expand_scatter write. Asynchronous on
+ * `stream`; the workspace must not be shared with a call that can overlap
+ * this one. Errors: as the two calls it replaces.
+ */
+int moe_expand_layout_scatter(const int32_t* topk_ids, const float* topk_w, const uint8_t* x,
+                              const void* x_scale, int scale_layout, int64_t ld_xs, int64_t T,
+                              int H, int K, int E, int align, const int32_t* d_n_valid,
+                              int64_t M_cap, int32_t* psum, int32_t* start, int32_t* d_total,
+                              int32_t* m_indices, int32_t* src2dst, int32_t* tile_prefix,
+                              uint8_t* xe, void* xe_scale, int64_t ld_xes, float* row_w, void* ws,
+                              size_t ws_bytes, int32_t* d_status, moe_stream_t stream);
+
 /* Host. Bytes of the fixed scratch array moe_expand_layout_noalloc uses. */
 size_t moe_expand_layout_noalloc_max_scratch(void);
 

@@ -63,6 +63,16 @@ def test_argument_validation_without_a_device(capi):
     assert lib.moe_combine(None, None, None, None, 4, 100, 2, None, None) == capi.MOE_ERR_INVALID_ARG
     assert lib.moe_act_quant(None, 256, None, 0, 0, None, 16, None, None, 2, None,
                              None) == capi.MOE_ERR_INVALID_ARG
+    # the fused layout + scatter: null outputs, then H not a multiple of 128
+    assert lib.moe_expand_layout_scatter(None, None, None, None, 0, 4, 4, 512, 2, 8, 32, None, 64,
+                                         None, None, None, None, None, None, None, None, 4, None,
+                                         None, 0, None, None) == capi.MOE_ERR_INVALID_ARG
+    buf = (ctypes.c_int32 * 4096)()
+    p = ctypes.cast(buf, ctypes.c_void_p).value
+    assert lib.moe_expand_layout_scatter(p, p, p, p, 0, 4, 4, 500, 2, 8, 32, None, 64, p, p, p, p,
+                                         p, p, p, p, 4, p, p, 4096, None,
+                                         None) == capi.MOE_ERR_INVALID_ARG
+    assert b"multiple of 128" in lib.moe_last_error_string()
 
 
 def test_product_package_does_not_import_the_oracle():

@@ -116,3 +116,35 @@ def test_workload_full_size(mx, orc, cfg):
                              inp["w13"], inp["s13"])
     gu_rows = u16(layer.gateup[[int(s2d_h[t, k]) for t, k in pairs]])
     assert_bf16_close(gu_rows, ref_rows, f"{cfg.name} gate_up rows")
+
+
+@pytest.mark.parametrize("cfg", synth.CONFIGS, ids=lambda c: c.name)
+def test_fused_layout_scatter_full_size(mx, cfg):
+    """moe_expand_layout_scatter at full size (in the benchmark's launch
+    configuration) writes the same layout and the same expanded rows, bit for
+    bit, as moe_expand_layout followed by moe_expand_scatter."""
+    dev = torch.device("cuda")
+    d = synth.generate(cfg, device=dev)
+    nv = d["n_valid"]
+    n_valid = torch.tensor([nv], dtype=torch.int32, device=dev)
+    sl = mx.scale_layout_of(cfg.scale_mode)
+    M_cap = int(mx.expanded_capacity(cfg.T, cfg.K, cfg.E, cfg.align))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    lay = mx.expand_layout(d["topk_ids"], cfg.E, cfg.align, M_cap, n_valid=n_valid, status=status)
+    xe, xs, rw = mx.expand_scatter(d["x_q"], d["x_s"], sl, d["topk_w"], lay, n_valid=n_valid,
+                                   status=status)
+    lay2, xe2, xs2, rw2 = mx.expand_layout_scatter(d["x_q"], d["x_s"], sl, d["topk_ids"],
+                                                   d["topk_w"], cfg.E, cfg.align, M_cap,
+                                                   n_valid=n_valid, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    total = int(lay.total.item())
+    assert int(lay2.total.item()) == total
+    for k in ("psum", "start", "tile_prefix", "m_indices", "src2dst"):
+        assert torch.equal(getattr(lay, k), getattr(lay2, k)), k
+    assert torch.equal(xe[:total], xe2[:total])
+    assert torch.equal(rw[:total].view(torch.int32), rw2[:total].view(torch.int32))
+    if cfg.scale_mode == "f32":
+        assert torch.equal(xs[:total].view(torch.int32), xs2[:total].view(torch.int32))
+    else:
+        assert torch.equal(xs[:, :total], xs2[:, :total])

@@ -92,6 +92,111 @@ def test_scatter_bit_exact(mx, cases, name):
         assert np.array_equal(xs[:, :tot], ref["xe_s"][:, :tot])
 
 
+@pytest.mark.parametrize("name", NAMES)
+def test_layout_scatter_fused_bit_exact(mx, cases, name):
+    """moe_expand_layout_scatter (the layout fused into the scatter): the
+    oracle's layout and expanded rows bit for bit, into buffers filled with
+    garbage first, so every row below the total must have been written."""
+    c = cases[name]
+    cfg, g, ref = c["cfg"], c["g"], c["ref"]
+    H = cfg.H
+    xe = torch.full((c["M_cap"], H), 0xAB, dtype=torch.uint8, device="cuda")
+    xe_s = mx.new_scale(c["M_cap"], H // 128, c["sl"], "cuda")
+    xe_s.view(torch.int32).fill_(0x7FC0DEAD)
+    row_w = torch.full((c["M_cap"],), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay, xe, xe_s, row_w = mx.expand_layout_scatter(
+        g["x_q"], g["x_s"], c["sl"], g["topk_ids"], g["topk_w"], cfg.E, cfg.align, c["M_cap"],
+        n_valid=g["n_valid_dev"], status=status, xe=xe, xe_scale=xe_s, row_w=row_w)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    rl = ref["layout"]
+    assert int(lay.total.item()) == rl["total"]
+    for k in ("psum", "start", "tile_prefix", "m_indices", "src2dst"):
+        assert np.array_equal(getattr(lay, k).cpu().numpy(), rl[k]), k
+    tot = ref["total"]
+    assert np.array_equal(xe.cpu().numpy()[:tot], ref["xe"][:tot])
+    assert np.array_equal(row_w.cpu().numpy().view(np.uint32)[:tot], ref["row_w"].view(np.uint32)[:tot])
+    xs = xe_s.cpu().numpy()
+    if c["sl"] == 0:
+        assert np.array_equal(xs[:tot].view(np.uint32), ref["xe_s"][:tot].view(np.uint32))
+    else:
+        assert np.array_equal(xs[:, :tot], ref["xe_s"][:, :tot])
+
+
+# Inputs with several 2048-pair layout chunks (the parity workloads above fit
+# one), top-k values that do not divide 2048 (chunks that split a token's
+# pairs), empty experts, inactive rows and a garbage tail past n_valid.
+MULTI_CHUNK = (
+    synth.LayerConfig("chunks_k6_zipf", T=1000, H=512, I=128, E=16, K=6, align=64, seed=30,
+                      routing="zipf", zipf_s=1.2, zipf_zero_experts=3, inactive_frac=0.05),
+    synth.LayerConfig("chunks_k8_ue8m0", T=700, H=640, I=128, E=12, K=8, align=16, seed=31,
+                      scale_mode=synth.SCALE_UE8M0),
+    synth.LayerConfig("chunks_k5_padded", T=1600, H=512, I=128, E=10, K=5, align=128, seed=32,
+                      n_valid=900, garbage_tail=True),
+)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+@pytest.mark.parametrize("cfg", MULTI_CHUNK, ids=[c.name for c in MULTI_CHUNK])
+def test_layout_scatter_multi_chunk_bit_exact(mx, orc, cfg, fused):
+    """Layout and scatter over several chunks against the oracle, bit for
+    bit, through moe_expand_layout + moe_expand_scatter and through
+    moe_expand_layout_scatter."""
+    d = synth.generate(cfg, device="cpu")
+    inp = orc.to_numpy_inputs(d)
+    M_cap = orc.expanded_capacity(cfg.T * cfg.K, cfg.E, cfg.align)
+    nv = inp["n_valid"]
+    rl = orc.layout(inp["topk_ids"], cfg.E, cfg.align, nv, M_cap)
+    assert rl["rc"] == 0
+    sl = mx.scale_layout_of(cfg.scale_mode)
+    rxe, rxs, rrw = orc.scatter(inp["x_q"], inp["x_s"], inp["scale_layout"], inp["topk_w"], rl, nv,
+                                cfg.E, cfg.align, M_cap)
+    g = {k: v.cuda() for k, v in d.items() if isinstance(v, torch.Tensor)}
+    nvd = torch.tensor([nv], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if fused:
+        lay, xe, xe_s, row_w = mx.expand_layout_scatter(
+            g["x_q"], g["x_s"], sl, g["topk_ids"], g["topk_w"], cfg.E, cfg.align, M_cap,
+            n_valid=nvd, status=status)
+    else:
+        lay = mx.expand_layout(g["topk_ids"], cfg.E, cfg.align, M_cap, n_valid=nvd, status=status)
+        xe, xe_s, row_w = mx.expand_scatter(g["x_q"], g["x_s"], sl, g["topk_w"], lay,
+                                            n_valid=nvd, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    tot = rl["total"]
+    assert int(lay.total.item()) == tot
+    for k in ("psum", "start", "tile_prefix", "m_indices", "src2dst"):
+        assert np.array_equal(getattr(lay, k).cpu().numpy(), rl[k]), k
+    assert np.array_equal(xe.cpu().numpy()[:tot], rxe[:tot])
+    assert np.array_equal(row_w.cpu().numpy().view(np.uint32)[:tot], rrw.view(np.uint32)[:tot])
+    xs = xe_s.cpu().numpy()
+    if sl == 0:
+        assert np.array_equal(xs[:tot].view(np.uint32), rxs[:tot].view(np.uint32))
+    else:
+        assert np.array_equal(xs[:, :tot], rxs[:, :tot])
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_layer_fused_layout_scatter_matches_default(mx, cases, name):
+    """A layer built with fuse_layout_scatter=True gives the default layer's
+    output bit for bit (same GEMM inputs)."""
+    c = cases[name]
+    cfg, g = c["cfg"], c["g"]
+    nv = c["inp"]["n_valid"]
+    ys = []
+    for fuse in (False, True):
+        layer = mx.ExpandedMoELayer(g["w13"], g["s13"], g["w2"], g["s2"], K=cfg.K, align=cfg.align,
+                                    scale_mode=cfg.scale_mode, max_tokens=cfg.T,
+                                    fuse_layout_scatter=fuse)
+        y = layer.forward(g["x_q"], g["x_s"], g["topk_ids"], g["topk_w"], g["n_valid_dev"])
+        torch.cuda.synchronize()
+        assert layer.status.item() == 0
+        ys.append(y[:nv].clone())
+    assert torch.equal(ys[0], ys[1])
+
+
 @pytest.mark.parametrize("tile_flag", [0, 16, 32, 64], ids=["default", "bn128", "cta_pair", "per_kblock"])
 @pytest.mark.parametrize("name", NAMES)
 def test_gate_up_gemm(mx, cases, name, tile_flag):
