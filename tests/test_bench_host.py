@@ -65,3 +65,20 @@ def test_reference_arm_other_ranks_do_nothing():
     import bench
     res, rank = bench.run_reference(bench.parse_args(["--impl", "reference"]), 2, 1)
     assert res is None and rank == 1
+
+
+def test_launches_per_step():
+    """The gpu_launches claim: kernels one step launches in each mode."""
+    import argparse
+    import bench
+    a = lambda **kw: argparse.Namespace(**{"fuse_layout_scatter": False, "masked_max_m": 0, **kw})  # noqa: E731
+    big = synth.config_by_name("zipf_t16384_h7168")
+    dec = synth.config_by_name("decode_t256_h7168_ue8m0")
+    # layout 2 + scatter + gate_up(+act+quant) + down + combine
+    assert bench.launches_per_step(a(), big, True) == 6
+    assert bench.launches_per_step(a(), big, False) == 7            # + stand-alone act_quant
+    assert bench.launches_per_step(a(masked_max_m=1152), big, True) == 8  # + two slab bridges
+    assert bench.launches_per_step(a(fuse_layout_scatter=True), big, True) == 5
+    # 256 x 8 pairs fit one 2048-pair chunk: the layout is one launch
+    assert bench.launches_per_step(a(), dec, True) == 5
+    assert bench.launches_per_step(a(fuse_layout_scatter=True), dec, True) == 5
