@@ -6,11 +6,16 @@ of the Zipf-routed T=16384, H=7168, I=2048, E=32, top-8 workload (the
 configuration the layer's targets are stated on), inputs resident in HBM.
 
 Prints one JSON line. ``value`` is whole-job tokens/s (valid tokens of all
-ranks / max-over-ranks time); ``roofline`` is for the dominant kernel (the
+ranks / max-over-ranks median step time; ``ms_per_step`` is that median and
+``ms_per_step_mean`` the mean); ``roofline`` is for the dominant kernel (the
 gate_up GEMM) from CUDA events around its launches in the timed region;
-``e2e`` is the same metric through ExpandedMoELayer.forward with the inputs
-copied from pinned host memory and the output copied back every step;
-``cpu_baseline`` is the CPU oracle on a sample of the same workload.
+``graph_replay`` times the same forward as one CUDA graph per step; ``e2e``
+is the same metric through the package's HostPipeline with each step's
+valid input rows copied from pinned host memory and its output rows copied
+back; ``cpu_baseline`` is the CPU oracle on a sample of the same workload,
+single-threaded and (``all_cores``) on a thread pool over the host cores;
+``per_config`` holds the median step time and per-kernel split of the other
+four workloads, measured in the same process after the headline one.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -75,6 +80,11 @@ def parse_args(argv=None):
                     help="force 128-column GEMM tiles (tuning comparison)")
     ap.add_argument("--gemm-cta-pair", action="store_true",
                     help="256 x 256 GEMM tiles on CTA pairs (tuning comparison)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload lines of the other four workloads")
+    ap.add_argument("--per-config-steps", type=int, default=10)
+    ap.add_argument("--no-graph-extra", action="store_true",
+                    help="skip the CUDA-graph replay timing added beside the eager step time")
     return ap.parse_args(argv)
 
 
@@ -211,33 +221,19 @@ def launches_per_step(args, cfg, fused: bool) -> int:
     ffn = 4 if args.masked_max_m else (2 if fused else 3)
     return front + ffn + 1
 
-def run_ours(args, world, rank, local):
-    import expanded_layout_expert_gb300 as mx
-    from expanded_layout_expert_gb300 import build as libbuild
 
-    libbuild.build()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    init_dist(world, "nccl")
-    cfg = rank_config(synth.config_by_name(args.workload), rank)
-    d = synth.generate(cfg, device=dev)
-    nv = d["n_valid"]
-    n_valid = torch.tensor([nv], dtype=torch.int32, device=dev)
-    layer = mx.ExpandedMoELayer(d["w13"], d["s13"], d["w2"], d["s2"], K=cfg.K, align=cfg.align,
-                                scale_mode=cfg.scale_mode, max_tokens=cfg.T, weighting=args.weighting,
-                                masked_max_m=args.masked_max_m or None,
-                                fuse_layout_scatter=args.fuse_layout_scatter)
-    L = mx.load()
-    stream = torch.cuda.current_stream()
+KERNEL_NAMES = ["layout", "scatter", "gemm1", "act_quant", "gemm2", "combine"]
+
+
+def make_step(args, cfg, layer, d, n_valid, mx, L, stream):
+    """One layer pass as direct C-ABI calls on `stream`; step(ev) records
+    events ev[0..6] around the six stages when given. Returns (step, fused)."""
     s = stream.cuda_stream
     lay = layer.lay
     ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
     x_q, x_s, ids, w = d["x_q"], d["x_s"], d["topk_ids"], d["topk_w"]
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    names = ["layout", "scatter", "gemm1", "act_quant", "gemm2", "combine"]
     gflags = (mx.MOE_GEMM_TILE_N128 if args.gemm_tile_n128 else 0) | \
         (mx.MOE_GEMM_CTA_PAIR if args.gemm_cta_pair else 0)
-
     # gate_up carries silu*mul, the quantiser and the fold in its epilogue
     fused = not args.unfused and gflags == 0
 
@@ -336,14 +332,108 @@ def run_ours(args, world, rank, local):
                                cfg.H, cfg.K, ptr(layer.y), s), "combine")
         mark(6)
 
+    return step, fused
+
+
+def timed_steps(step, stream, steps: int, flush):
+    """`steps` passes with L2 flushed between them (outside the events).
+    Returns (per-step ms list, per-kernel ms lists)."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for k in range(steps):
+        flush.fill_(k & 0xFF)          # evict the previous step's data from L2
+        step(evs[k])
+    torch.cuda.synchronize()
+    per_kernel = {n: [ev[i].elapsed_time(ev[i + 1]) for ev in evs] for i, n in enumerate(KERNEL_NAMES)}
+    return [ev[0].elapsed_time(ev[6]) for ev in evs], per_kernel
+
+
+def layer_work(layer, cfg, nv):
+    lay = layer.lay
+    psum = lay.psum.cpu().numpy()
+    start = lay.start.cpu().numpy()
+    P = int((psum - start).sum())
+    M_pad = int(lay.total.item())
+    return P, M_pad, algorithmic_work(cfg, P, M_pad, nv)
+
+
+def kernel_split(per_kernel_ms, work, fused, args, hbm, fp8_peak):
+    """Per stage: mean and median ms, achieved GB/s or TFLOP/s (from the
+    mean, the average launch duration) and the fraction of the measured peak."""
+    kernels = {}
+    for n in KERNEL_NAMES:
+        ms = statistics.mean(per_kernel_ms[n])
+        med = statistics.median(per_kernel_ms[n])
+        if fused and n == "act_quant":
+            kernels[n] = {"ms": 0.0, "fused_into": "gemm1"}
+            continue
+        if args.fuse_layout_scatter and n == "layout":
+            kernels[n] = {"ms": 0.0, "fused_into": "scatter"}
+            continue
+        if n.startswith("gemm"):
+            ach = work[n] / (ms / 1e3) / 1e12
+            kernels[n] = {"ms": round(ms, 4), "ms_median": round(med, 4), "achieved": round(ach, 1),
+                          "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4), "work": work[n]}
+        else:
+            ach = work[n] / (ms / 1e3) / 1e9
+            kernels[n] = {"ms": round(ms, 4), "ms_median": round(med, 4), "achieved": round(ach, 1),
+                          "unit": "GB/s", "frac": round(ach / hbm, 4), "work": work[n]}
+    return kernels
+
+
+def run_workload(args, mx, L, cfg, dev, stream, flush, steps):
+    """Builds the layer for one workload, warms up, times `steps` steps.
+    Returns a dict of the timing plus the objects a caller may reuse."""
+    d = synth.generate(cfg, device=dev)
+    nv = d["n_valid"]
+    n_valid = torch.tensor([nv], dtype=torch.int32, device=dev)
+    layer = mx.ExpandedMoELayer(d["w13"], d["s13"], d["w2"], d["s2"], K=cfg.K, align=cfg.align,
+                                scale_mode=cfg.scale_mode, max_tokens=cfg.T, weighting=args.weighting,
+                                masked_max_m=args.masked_max_m or None,
+                                fuse_layout_scatter=args.fuse_layout_scatter)
+    step, fused = make_step(args, cfg, layer, d, n_valid, mx, L, stream)
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
     if layer.status.item() != 0:
-        raise RuntimeError(f"device status {layer.status.item()} after warm-up")
+        raise RuntimeError(f"device status {layer.status.item()} after warm-up ({cfg.name})")
+    return dict(d=d, nv=nv, n_valid=n_valid, layer=layer, step=step, fused=fused)
+
+
+def graph_replay_ms(layer, d, n_valid, stream, flush, steps: int):
+    """Median time of one CUDA-graph replay of the whole forward (L2 flushed
+    between replays, outside the events)."""
+    cap = layer.capture(d["x_q"], d["x_s"], d["topk_ids"], d["topk_w"], n_valid)
+    cap.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for k, (a, b) in enumerate(evs):
+        flush.fill_(k & 0xFF)
+        a.record(stream)
+        cap.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def run_ours(args, world, rank, local):
+    import expanded_layout_expert_gb300 as mx
+    from expanded_layout_expert_gb300 import build as libbuild
+
+    libbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    init_dist(world, "nccl")
+    cfg = rank_config(synth.config_by_name(args.workload), rank)
+    L = mx.load()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    run = run_workload(args, mx, L, cfg, dev, stream, flush, args.steps)
+    d, nv, n_valid, layer, fused = run["d"], run["nv"], run["n_valid"], run["layer"], run["fused"]
+    step = run["step"]
 
     if args.graph:
-        cap = layer.capture(x_q, x_s, ids, w, n_valid)
+        cap = layer.capture(d["x_q"], d["x_s"], d["topk_ids"], d["topk_w"], n_valid)
         cap.replay()
         torch.cuda.synchronize()
 
@@ -355,66 +445,36 @@ def run_ours(args, world, rank, local):
             if ev is not None:
                 ev[6].record(stream)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     with ClockSampler(local) as clocks:
-        for k in range(args.steps):
-            flush.fill_(k & 0xFF)          # evict the previous step's data from L2
-            step(evs[k])
-        torch.cuda.synchronize()
+        step_list, per_kernel = timed_steps(step, stream, args.steps, flush)
     barrier(world)
     t_wall = time.perf_counter() - t_wall0
-    per_kernel = {n: 0.0 for n in names}
-    step_ms = 0.0
-    for ev in evs:
-        for i, n in enumerate(names):
-            per_kernel[n] += ev[i].elapsed_time(ev[i + 1])
-        step_ms += ev[0].elapsed_time(ev[6])
-    step_ms /= args.steps
-    per_kernel = {n: v / args.steps for n, v in per_kernel.items()}
     if layer.status.item() != 0:
         raise RuntimeError(f"device status {layer.status.item()} in the timed region")
+    step_med = statistics.median(step_list)
+    step_mean = statistics.mean(step_list)
 
-    psum = lay.psum.cpu().numpy()
-    start = lay.start.cpu().numpy()
-    P = int((psum - start).sum())
-    M_pad = int(lay.total.item())
-    work = algorithmic_work(cfg, P, M_pad, nv)
-
-    step_ms_max = reduce_max(step_ms, world, dev)
+    P, M_pad, work = layer_work(layer, cfg, nv)
+    step_ms_max = reduce_max(step_med, world, dev)
     tokens_all = reduce_sum(float(nv), world, dev)
     value = tokens_all / (step_ms_max / 1e3)
 
     peaks, peak_src = load_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     fp8_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * FP8_PER_BF16
-    kernels = {}
-    for n in ([] if args.graph else names):
-        ms = per_kernel[n]
-        if fused and n == "act_quant":
-            kernels[n] = {"ms": 0.0, "fused_into": "gemm1"}
-            continue
-        if args.fuse_layout_scatter and n == "layout":
-            kernels[n] = {"ms": 0.0, "fused_into": "scatter"}
-            continue
-        if n.startswith("gemm"):
-            ach = work[n] / (ms / 1e3) / 1e12
-            kernels[n] = {"ms": round(ms, 4), "achieved": round(ach, 1), "unit": "TFLOP/s",
-                          "frac": round(ach / fp8_peak, 4), "work": work[n]}
-        else:
-            ach = work[n] / (ms / 1e3) / 1e9
-            kernels[n] = {"ms": round(ms, 4), "achieved": round(ach, 1), "unit": "GB/s",
-                          "frac": round(ach / hbm, 4), "work": work[n]}
     if args.graph:
-        kernels = {"graph_replay": {"ms": round(step_ms, 4)}}
+        kernels = {"graph_replay": {"ms": round(step_med, 4)}}
         sc_gbs = gemm_tflops = float("nan")
         roofline = None
     else:
+        kernels = kernel_split(per_kernel, work, fused, args, hbm, fp8_peak)
+        pk = {n: statistics.mean(v) for n, v in per_kernel.items()}
         sc_bytes = work["scatter"] + work["combine"]
-        sc_gbs = sc_bytes / ((per_kernel["scatter"] + per_kernel["combine"]) / 1e3) / 1e9
-        gemm_tflops = (work["gemm1"] + work["gemm2"]) / ((per_kernel["gemm1"] + per_kernel["gemm2"]) / 1e3) / 1e12
+        sc_gbs = sc_bytes / ((pk["scatter"] + pk["combine"]) / 1e3) / 1e9
+        gemm_tflops = (work["gemm1"] + work["gemm2"]) / ((pk["gemm1"] + pk["gemm2"]) / 1e3) / 1e12
         roofline = {"bound": "tensor",
                     "kernel": "grouped_gemm (gate_up" + (" + act_quant epilogue)" if fused else ")"),
                     "achieved": kernels["gemm1"]["achieved"], "peak": round(fp8_peak, 1),
@@ -425,20 +485,10 @@ def run_ours(args, world, rank, local):
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms_max, 4),
+        "ms_per_step_mean": round(step_mean, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3",
         "data": "synthetic (seeded generator; no dataset or trained weights)",
-        "config": {"workload": cfg.name, "T": cfg.T, "n_valid": nv, "H": cfg.H, "I": cfg.I,
-                   "E": cfg.E, "top_k": cfg.K, "expert_alignment": cfg.align,
-                   "routing": (f"zipf(s={cfg.zipf_s}), {cfg.zipf_zero_experts} experts empty"
-                               if cfg.routing == "zipf" else cfg.routing),
-                   "inactive_rows": cfg.inactive_frac, "scales": cfg.scale_mode,
-                   "weighting": args.weighting,
-                   "masked_max_m": args.masked_max_m or None,
-                   "cuda_graph": bool(args.graph),
-                   "layout_scatter": "one call, 2 launches" if args.fuse_layout_scatter else "2 calls",
-                   "valid_pairs": P, "expanded_rows": M_pad, "M_cap": layer.M_cap,
-                   "l2": "flushed between steps (256 MiB write outside the timed events)",
-                   "parallelism": f"replicas x{world} (token-sharded, no collective)"},
+        "config": workload_config(cfg, nv, P, M_pad, layer, args, world),
         "scatter_combine_gbs": None if args.graph else round(sc_gbs, 1),
         "grouped_fp8_tflops": None if args.graph else round(gemm_tflops, 1),
         "kernels": kernels,
@@ -448,12 +498,64 @@ def run_ours(args, world, rank, local):
         "wall_s_timed_region": round(t_wall, 3),
     }
 
+    if not args.graph and not args.no_graph_extra:
+        gms = graph_replay_ms(layer, d, n_valid, stream, flush, max(10, args.steps))
+        result["graph_replay"] = {"ms_per_step": round(gms, 4),
+                                  "tokens_per_s": round(nv / (gms / 1e3), 1),
+                                  "steps": max(10, args.steps),
+                                  "how": "one CUDA graph of the whole forward per step; "
+                                         "median; L2 flushed between replays"}
+
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, layer, d, dev, world)
 
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"], result["parity_sample"] = run_cpu_baseline(args, cfg, d, layer)
+
+    if rank == 0 and not args.no_per_config and not args.graph:
+        del run, step, layer, d
+        torch.cuda.empty_cache()
+        result["per_config"] = run_per_config(args, mx, L, dev, stream, flush, hbm, fp8_peak,
+                                              exclude=cfg.name)
     return result, rank
+
+
+def workload_config(cfg, nv, P, M_pad, layer, args, world):
+    return {"workload": cfg.name, "T": cfg.T, "n_valid": nv, "H": cfg.H, "I": cfg.I,
+            "E": cfg.E, "top_k": cfg.K, "expert_alignment": cfg.align,
+            "routing": (f"zipf(s={cfg.zipf_s}), {cfg.zipf_zero_experts} experts empty"
+                        if cfg.routing == "zipf" else cfg.routing),
+            "inactive_rows": cfg.inactive_frac, "scales": cfg.scale_mode,
+            "weighting": args.weighting,
+            "masked_max_m": args.masked_max_m or None,
+            "cuda_graph": bool(args.graph),
+            "layout_scatter": "one call, 2 launches" if args.fuse_layout_scatter else "2 calls",
+            "valid_pairs": P, "expanded_rows": M_pad, "M_cap": layer.M_cap,
+            "l2": "flushed between steps (256 MiB write outside the timed events)",
+            "parallelism": f"replicas x{world} (token-sharded, no collective)"}
+
+
+def run_per_config(args, mx, L, dev, stream, flush, hbm, fp8_peak, exclude):
+    """The other workloads, one after another in the same process: median
+    step time and the per-kernel split of `--per-config-steps` steps each."""
+    out = {}
+    for cfg in synth.CONFIGS:
+        if cfg.name == exclude:
+            continue
+        run = run_workload(args, mx, L, cfg, dev, stream, flush, args.per_config_steps)
+        steps, per_kernel = timed_steps(run["step"], stream, args.per_config_steps, flush)
+        if run["layer"].status.item() != 0:
+            raise RuntimeError(f"device status {run['layer'].status.item()} ({cfg.name})")
+        P, M_pad, work = layer_work(run["layer"], cfg, run["nv"])
+        med = statistics.median(steps)
+        out[cfg.name] = {
+            "ms_per_step": round(med, 4), "ms_per_step_mean": round(statistics.mean(steps), 4),
+            "tokens_per_s": round(run["nv"] / (med / 1e3), 1), "steps": args.per_config_steps,
+            "n_valid": run["nv"], "valid_pairs": P, "expanded_rows": M_pad, "scales": cfg.scale_mode,
+            "kernels": kernel_split(per_kernel, work, run["fused"], args, hbm, fp8_peak)}
+        del run
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, layer, d, dev, world):
@@ -461,18 +563,26 @@ def run_e2e(args, layer, d, dev, world):
     batches (HostPipeline over ExpandedMoELayer.forward): every step copies its
     inputs from pinned host memory and its output y back to pinned host
     memory inside the timed region; the copies of neighbouring steps overlap
-    the kernels on their own streams."""
+    the kernels on their own streams. The valid-row count is known on the
+    host, so only the valid rows travel (the padded buffer's garbage tail
+    stays where it is)."""
+    nv = d["n_valid"]
     host = {k: d[k].cpu().pin_memory() for k in ("x_q", "x_s", "topk_ids", "topk_w")}
-    nv_host = torch.tensor([d["n_valid"]], dtype=torch.int32).pin_memory()
+    nv_host = torch.tensor([nv], dtype=torch.int32).pin_memory()
     y_host = [torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory() for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host.values()) + 4
-    d2h = y_host[0].numel() * y_host[0].element_size()
+
+    def rows_bytes(t, n):
+        if t.shape[0] == layer.T:                 # row-major [T, ...]
+            return n * t[0].numel() * t.element_size()
+        return t.shape[0] * n * t.element_size()  # column-major packed scales [W, T]
+    h2d = sum(rows_bytes(t, nv) for t in host.values()) + 4
+    d2h = rows_bytes(y_host[0], nv)
     import expanded_layout_expert_gb300 as mx
     pipe = mx.HostPipeline(layer)
 
     def one(k):
         pipe.submit(host["x_q"], host["x_s"], host["topk_ids"], host["topk_w"], nv_host,
-                    y_host[k % 2])
+                    y_host[k % 2], n_rows=nv)
 
     for k in range(3):
         one(k)
@@ -485,18 +595,21 @@ def run_e2e(args, layer, d, dev, world):
     pipe.synchronize()
     ms = 1e3 * (time.perf_counter() - t0) / steps
     ms = reduce_max(ms, world, dev)
-    tokens = reduce_sum(float(d["n_valid"]), world, dev)
-    ok = torch.equal(y_host[(steps - 1) % 2][: d["n_valid"]], layer.y[: d["n_valid"]].cpu())
+    tokens = reduce_sum(float(nv), world, dev)
+    ok = torch.equal(y_host[(steps - 1) % 2][:nv], layer.y[:nv].cpu())
     return {"value": round(tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "output_matches_device_run": bool(ok),
-            "api": "HostPipeline(ExpandedMoELayer): pinned host batches, copies on their own "
-                   "streams overlapping the kernels; host wall clock, all streams synchronised"}
+            "api": "HostPipeline(ExpandedMoELayer), submit(..., n_rows=n_valid): pinned host "
+                   "batches, the valid rows copied on their own streams overlapping the kernels; "
+                   "host wall clock, all streams synchronised"}
 
 
-def _oracle_sample(cfg, d, seconds: float, t_list=None):
+def _oracle_sample(cfg, d, seconds: float, t_list=None, threads: int = 1):
     """The CPU oracle's per-token path on valid tokens of the workload for about
-    `seconds`; returns (tokens, elapsed, {t: y_row})."""
+    `seconds`; returns (tokens, elapsed, {t: y_row}). With threads > 1 the
+    tokens go to a thread pool (the oracle is C called through ctypes, which
+    releases the GIL while it runs)."""
     import oracle
     inp = oracle.to_numpy_inputs({k: v for k, v in d.items()})
     nv = inp["n_valid"]
@@ -505,11 +618,38 @@ def _oracle_sample(cfg, d, seconds: float, t_list=None):
     order = t_list if t_list is not None else active[:: max(1, len(active) // 997)]
     out = {}
     t0 = time.perf_counter()
-    for t in order:
-        out[t] = oracle.token_forward(inp, t)
-        if time.perf_counter() - t0 > seconds:
-            break
+    if threads <= 1:
+        for t in order:
+            out[t] = oracle.token_forward(inp, t)
+            if time.perf_counter() - t0 > seconds:
+                break
+        return len(out), time.perf_counter() - t0, out
+    import concurrent.futures as cf
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        it = iter(order)
+        pending = set()
+        for _ in range(threads):
+            t = next(it, None)
+            if t is not None:
+                pending.add(ex.submit(lambda t=t: (t, oracle.token_forward(inp, t))))
+        while pending:
+            done, pending = cf.wait(pending, return_when=cf.FIRST_COMPLETED)
+            for f in done:
+                t, y = f.result()
+                out[t] = y
+            if time.perf_counter() - t0 <= seconds:
+                for _ in done:
+                    t = next(it, None)
+                    if t is not None:
+                        pending.add(ex.submit(lambda t=t: (t, oracle.token_forward(inp, t))))
     return len(out), time.perf_counter() - t0, out
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
 
 
 def run_cpu_baseline(args, cfg, d, layer):
@@ -523,6 +663,14 @@ def run_cpu_baseline(args, cfg, d, layer):
     base = {"value": round(n / secs, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{n} valid tokens of {cfg.name} through the oracle's per-token path "
                       f"(single-threaded C, fp64), {secs:.1f} s"}
+    cores = host_cores()
+    if cores > 1 and args.cpu_sample_seconds > 0:
+        n2, secs2, _ = _oracle_sample(cfg, d, args.cpu_sample_seconds, threads=cores)
+        base["all_cores"] = {"value": round(n2 / secs2, 3), "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"{n2} valid tokens of {cfg.name}, the same per-token path "
+                                       f"on a pool of {cores} threads (one token each), "
+                                       f"{secs2:.1f} s"}
     return base, {"tokens": n, "rel_fro": fro, "max_abs": mx}
 
 

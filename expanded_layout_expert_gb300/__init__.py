@@ -461,6 +461,13 @@ class HostPipeline:
     Host tensors must be pinned (page-locked) for the copies to be
     asynchronous, and a y_host may be read only after synchronize() (or after
     the submit two batches later has returned and its event completed).
+
+    submit(..., n_rows=n) is for callers that know on the host how many
+    leading rows of the batch are valid (n >= the n_valid the device word
+    holds): only rows [0, n) of x_q, x_scale, topk_ids, topk_w go to the
+    device and only rows [0, n) of y come back. The layer itself still takes
+    the valid-row count from the device word; rows past it are never read,
+    so what the device buffers hold there does not matter.
     """
 
     def __init__(self, layer: "ExpandedMoELayer", stream=None):
@@ -485,18 +492,29 @@ class HostPipeline:
         self.out_copied = [torch.cuda.Event() for _ in range(2)]
         self.k = 0
 
-    def submit(self, x_q, x_scale, topk_ids, topk_w, n_valid, y_host) -> None:
+    def submit(self, x_q, x_scale, topk_ids, topk_w, n_valid, y_host,
+               n_rows: Optional[int] = None) -> None:
         i = self.k % 2
         b = self.bufs[i]
         if b["x_s"].shape != x_scale.shape:
             raise ValueError("x_scale shape does not match the layer's scale layout")
+        T = self.layer.T
+        n = T if n_rows is None else int(n_rows)
+        if not 0 <= n <= T:
+            raise ValueError(f"n_rows must be in [0, {T}], got {n}")
         with torch.cuda.stream(self.h2d):
             if self.k >= 2:
                 self.h2d.wait_event(self.done[i])      # batch k-2 has read these inputs
-            b["x_q"].copy_(x_q, non_blocking=True)
-            b["x_s"].copy_(x_scale, non_blocking=True)
-            b["ids"].copy_(topk_ids, non_blocking=True)
-            b["w"].copy_(topk_w, non_blocking=True)
+            b["x_q"][:n].copy_(x_q[:n], non_blocking=True)
+            if self.layer.sl == MOE_SCALE_F32_ROWMAJOR:
+                b["x_s"][:n].copy_(x_scale[:n], non_blocking=True)
+            elif n == T:
+                b["x_s"].copy_(x_scale, non_blocking=True)
+            else:
+                for j in range(x_scale.shape[0]):      # column-major: one run per word row
+                    b["x_s"][j, :n].copy_(x_scale[j, :n], non_blocking=True)
+            b["ids"][:n].copy_(topk_ids[:n], non_blocking=True)
+            b["w"][:n].copy_(topk_w[:n], non_blocking=True)
             b["nv"].copy_(n_valid, non_blocking=True)
             self.in_ready[i].record(self.h2d)
         self.comp.wait_event(self.in_ready[i])
@@ -507,7 +525,7 @@ class HostPipeline:
         self.done[i].record(self.comp)
         with torch.cuda.stream(self.d2h):
             self.d2h.wait_event(self.done[i])
-            y_host.copy_(b["y"], non_blocking=True)
+            y_host[:n].copy_(b["y"][:n], non_blocking=True)
             self.out_copied[i].record(self.d2h)
         self.k += 1
 

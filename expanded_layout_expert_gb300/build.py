@@ -79,5 +79,38 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     return LIB
 
 
+def ptxas_usage(source: str) -> dict:
+    """Compiles one csrc/ source for sm_103a with -Xptxas -v (object to a
+    temporary file) and returns, per kernel entry, the registers and the
+    bytes of stack frame, spill stores and spill loads ptxas reports."""
+    import re
+    import tempfile
+    src = os.path.join(CSRC, source)
+    with tempfile.TemporaryDirectory() as tmp:
+        cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, "-Xptxas", "-v", "-c", src,
+               "-o", os.path.join(tmp, "k.o")]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on {source}:\n{r.stdout}\n{r.stderr}")
+    out, cur = {}, None
+    for line in (r.stdout + r.stderr).splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            cur = m.group(1)
+            out[cur] = {}
+            continue
+        if cur is None:
+            continue
+        m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads",
+                      line)
+        if m:
+            out[cur].update(stack=int(m.group(1)), spill_st=int(m.group(2)),
+                            spill_ld=int(m.group(3)))
+        m = re.search(r"Used (\d+) registers", line)
+        if m:
+            out[cur]["registers"] = int(m.group(1))
+    return out
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))

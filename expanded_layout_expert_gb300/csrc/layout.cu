@@ -438,10 +438,33 @@ constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB per device
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch, looked up once per device. In host
-// code the array's name is only a host-side stand-in, never the device
-// address, so kernels must be given this pointer instead.
-void* g_noalloc_addr[64] = {};
+// Device address of g_noalloc_scratch, looked up once per device and CUDA
+// context. In host code the array's name is only a host-side stand-in, never
+// the device address, so kernels must be given this pointer instead. The
+// cache is keyed on the current context as well as the device: after a
+// device reset (or the primary context's teardown) the module is loaded
+// again, the array may sit at another address, and the lookup is redone.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  });
+  return fn;
+}
+
+struct NoAllocSlot {
+  CUcontext ctx = nullptr;
+  void* addr = nullptr;
+};
+NoAllocSlot g_noalloc_slot[64];
 std::mutex g_noalloc_mu;
 
 int noalloc_scratch(void** out) {
@@ -455,17 +478,29 @@ int noalloc_scratch(void** out) {
     set_error("moe_expand_layout_noalloc: device index %d out of range", dev);
     return MOE_ERR_UNSUPPORTED;
   }
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (get_ctx == nullptr) {
+    set_error("moe_expand_layout_noalloc: cuCtxGetCurrent is not available from the driver");
+    return MOE_ERR_CUDA;
+  }
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+    set_error("moe_expand_layout_noalloc: no current CUDA context");
+    return MOE_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
+  NoAllocSlot& slot = g_noalloc_slot[dev];
+  if (slot.addr == nullptr || slot.ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
       set_error("moe_expand_layout_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
       return MOE_ERR_CUDA;
     }
-    g_noalloc_addr[dev] = p;
+    slot.ctx = ctx;
+    slot.addr = p;
   }
-  *out = g_noalloc_addr[dev];
+  *out = slot.addr;
   return MOE_OK;
 }
 
@@ -494,14 +529,22 @@ extern "C" int moe_expand_layout_noalloc(const int32_t* topk_ids, int64_t T, int
               "the fixed %zu; use moe_expand_layout with a workspace",
               (long long)T, K, E, need, moe::kNoAllocScratchBytes);
   MOE_REQUIRE_DEVICE();
+  const int nb = static_cast<int>(moe::num_chunks(T, K));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (nb == 1) {
+    // every pair in one chunk: the one-launch layout, which needs no scratch
+    const size_t smem = static_cast<size_t>(moe::kWarps + 2) * E * sizeof(int);
+    moe::layout_single_kernel<<<1, moe::kThreads, smem, s>>>(topk_ids, T, K, E, align, d_n_valid,
+                                                            M_cap, psum, start, d_total, tile_prefix,
+                                                            m_indices, src2dst, d_status);
+    return moe::check_launch("layout_single_kernel");
+  }
   void* ws = nullptr;
   int rc = moe::noalloc_scratch(&ws);
   if (rc != MOE_OK) return rc;
-  const int nb = static_cast<int>(moe::num_chunks(T, K));
   int32_t* counts = static_cast<int32_t*>(ws);
   int32_t* offs = counts + static_cast<int64_t>(E) * nb;
   unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + need - 256);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // The array keeps whatever the previous call left; the ticket must start
   // at zero (the counts and offsets are fully rewritten every call).
   cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);

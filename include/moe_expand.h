@@ -83,7 +83,10 @@ int64_t moe_expanded_capacity(int64_t T, int K, int E, int align);
 
 /* Host. Bytes of device workspace moe_expand_layout needs for (T, K, E).
  * The workspace must be zero-filled once before its first use; every
- * successful call leaves it ready for the next call. */
+ * successful call leaves it ready for the next call. It holds per-(expert,
+ * 2048-pair chunk) counts and offsets and a completion ticket, so its size
+ * depends on T*K and E only; unlike a workspace sized by the expanded
+ * capacity, it takes no M_cap argument. */
 size_t moe_workspace_size(int64_t T, int K, int E);
 
 /*
@@ -122,16 +125,22 @@ int moe_expand_layout(const int32_t* topk_ids, int64_t T, int K, int E, int alig
  * the device. Arguments and outputs are those of moe_expand_layout.
  *  - Scratch: a fixed 1 MiB array in the library's device image, held by
  *    every GPU that loads the library until the process exits. A call needs
- *    moe_workspace_size(T, K, E) bytes of it (2*E*ceil(T*K/2048)*4 bytes
- *    rounded up to 256, plus 256: E = 32 fits up to 8.3 M (token, expert)
- *    pairs, E = 1024 up to 258 k); larger sizes are rejected with
- *    MOE_ERR_INVALID_ARG and a message, before any device work.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    moe_workspace_size(T, K, E) bytes of it: 8*E bytes per chunk of 2048
+ *    (token, expert) pairs, rounded up to 256, plus 256. So it holds at most
+ *    floor((2^20 - 256) / (8*E)) chunks: 4095 chunks (8,386,560 pairs) at
+ *    E = 32, 127 chunks (260,096 pairs) at E = 1024. Larger sizes are
+ *    rejected with MOE_ERR_INVALID_ARG and a message, before any device work.
+ *  - When all pairs fit one chunk (T*K <= 2048, a decode-sized batch) the
+ *    call is the single launch moe_expand_layout also uses there; it touches
+ *    no scratch, no lookup and no memset.
+ *  - Otherwise the first call on a device looks up the array's device
+ *    address (cudaGetSymbolAddress) with that device current, and again
+ *    whenever the current CUDA context of the device has changed (after a
+ *    device reset); make that first call before any stream capture.
  *  - Every call shares the one array and it keeps the last call's contents;
  *    the call clears the part that must start at zero (an asynchronous 4-byte
- *    memset on the stream). Calls that overlap on the GPU (different streams,
+ *    memset on the stream). Calls ordered on one stream may follow each other
+ *    without a host wait. Calls that overlap on the GPU (different streams,
  *    no ordering between them) race on the array and give wrong results.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
@@ -194,7 +203,15 @@ int moe_expand_scatter(const uint8_t* x, const void* x_scale, int scale_layout, 
  *   A_scale  device, scale_layout, leading dimension ld_as
  *   W        device uint8 [E, N, Kd] K-major ("nt"); W_scale fp32 [E, N/128, Kd/128]
  *            (scale_layout F32) or uint8 ue8m0 bytes (scale_layout UE8M0)
- *   start, tile_prefix, d_total: from moe_expand_layout
+ *   start, tile_prefix, d_total: from moe_expand_layout. The GEMM takes the
+ *            segment starts and the per-expert 128-row tile prefix, not the
+ *            per-row m_indices labels: a persistent CTA turns a linear tile
+ *            id into (expert, m block) by a binary search over E+1 prefix
+ *            entries kept in shared memory, and the tile count comes from
+ *            the prefix's last entry, which a per-row label array cannot
+ *            give without a scan. m_indices stays a layout output for
+ *            callers whose GEMM reads per-row labels (DeepGEMM's contiguous
+ *            layout); nothing in this library reads it.
  *   row_w    device fp32 [M_cap], read only with MOE_WEIGHT_OUTPUT_ROWS
  *   out      device bf16 [M_cap, N]
  * With MOE_WEIGHT_OUTPUT_ROWS the sum is multiplied by row_w[r] before the

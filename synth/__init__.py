@@ -125,6 +125,13 @@ PARITY_CONFIGS = (
     # per-K-block promotion kernel
     LayerConfig("small_h384_ue8m0", T=64, H=384, I=128, E=6, K=2, align=8, seed=18,
                 routing="uniform", scale_mode=SCALE_UE8M0, inactive_frac=0.10),
+    # the full workloads' hidden size: 56 K blocks in gate_up, so every row of
+    # a long-K GEMM (accumulator ring and scale words wrapping many times) is
+    # compared with the oracle
+    LayerConfig("longk_h7168", T=64, H=7168, I=256, E=4, K=2, align=32, seed=19,
+                routing="uniform", inactive_frac=0.05),
+    LayerConfig("longk_h7168_ue8m0", T=48, H=7168, I=256, E=4, K=2, align=16, seed=21,
+                routing="uniform", scale_mode=SCALE_UE8M0),
 )
 
 

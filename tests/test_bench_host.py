@@ -82,3 +82,16 @@ def test_launches_per_step():
     # 256 x 8 pairs fit one 2048-pair chunk: the layout is one launch
     assert bench.launches_per_step(a(), dec, True) == 5
     assert bench.launches_per_step(a(fuse_layout_scatter=True), dec, True) == 5
+
+
+def test_oracle_sample_on_a_thread_pool_matches_one_thread():
+    """The all-cores CPU baseline runs the oracle's per-token path on a
+    thread pool; the rows it returns are the single-threaded ones."""
+    import bench
+    cfg = synth.config_by_name("tiny_h512")
+    d = synth.generate(cfg)
+    toks = list(range(12))
+    n1, _, y1 = bench._oracle_sample(cfg, d, 600.0, t_list=toks)
+    n2, _, y2 = bench._oracle_sample(cfg, d, 600.0, t_list=toks, threads=4)
+    assert n1 == n2 == len(toks)
+    assert all((y1[t] == y2[t]).all() for t in toks)

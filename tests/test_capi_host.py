@@ -83,3 +83,21 @@ def test_product_package_does_not_import_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "moe_oracle" not in src, f
+
+
+def test_noalloc_scratch_limit(capi):
+    """moe_expand_layout_noalloc's fixed array holds floor((2^20 - 256) / 8E)
+    chunks of 2048 pairs; one pair more is refused before any device work."""
+    lib = capi.load()
+    cap = lib.moe_expand_layout_noalloc_max_scratch()
+    assert cap == 1 << 20
+    buf = (ctypes.c_int32 * 16)()
+    p = ctypes.cast(buf, ctypes.c_void_p).value
+    for E, nb_max in ((32, 4095), (1024, 127)):
+        assert nb_max == (cap - 256) // (8 * E)
+        assert lib.moe_workspace_size(nb_max * 2048, 1, E) <= cap
+        assert lib.moe_workspace_size(nb_max * 2048 + 1, 1, E) > cap
+        rc = lib.moe_expand_layout_noalloc(p, nb_max * 2048 + 1, 1, E, 128, None, 64, p, p, p, p,
+                                           p, p, None, None)
+        assert rc == capi.MOE_ERR_INVALID_ARG
+        assert b"scratch" in lib.moe_last_error_string()

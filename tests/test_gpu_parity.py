@@ -72,24 +72,73 @@ def test_layout_bit_exact(mx, cases, name):
         assert np.array_equal(getattr(lay, k).cpu().numpy(), ref[k]), k
 
 
+def _poisoned_scatter_buffers(mx, M_cap, H, sl):
+    """Expanded buffers holding garbage: 0xAB codes, NaN scale bits (fp32) or
+    all-ones packed words (ue8m0), NaN weights."""
+    xe = torch.full((M_cap, H), 0xAB, dtype=torch.uint8, device="cuda")
+    xe_s = mx.new_scale(M_cap, H // 128, sl, "cuda")
+    xe_s.view(torch.int32).fill_(0x7FC0DEAD if sl == 0 else -1)
+    row_w = torch.full((M_cap,), float("nan"), dtype=torch.float32, device="cuda")
+    return xe, xe_s, row_w
+
+
+def _assert_scatter_equal(xe, xe_s, row_w, sl, rxe, rxs, rrw, tot, what):
+    assert np.array_equal(xe.cpu().numpy()[:tot], rxe[:tot]), f"{what}: rows"
+    assert np.array_equal(row_w.cpu().numpy().view(np.uint32)[:tot], rrw.view(np.uint32)[:tot]), \
+        f"{what}: weights"
+    xs = xe_s.cpu().numpy()
+    if sl == 0:
+        assert np.array_equal(xs[:tot].view(np.uint32), rxs[:tot].view(np.uint32)), f"{what}: scales"
+    else:
+        assert np.array_equal(xs[:, :tot], rxs[:, :tot]), f"{what}: packed scales"
+
+
+def _rotated_routing(ids: np.ndarray, E: int) -> np.ndarray:
+    """A second routing of the same tokens: every valid id moved to the next
+    expert (the -1 entries stay), so the segment boundaries move."""
+    return np.where(ids >= 0, (ids + 1) % E, ids).astype(np.int32)
+
+
 @pytest.mark.parametrize("name", NAMES)
-def test_scatter_bit_exact(mx, cases, name):
+def test_scatter_bit_exact(mx, orc, cases, name):
+    """The default moe_expand_scatter into buffers full of garbage: every row
+    below the total, alignment gaps included, equals the oracle's scatter bit
+    for bit (codes, scales or packed scale words, weights). Then the same
+    buffers take a second routing, so that rows which held token data become
+    gaps and must be zeroed (vLLM PR 54109, Motivation: the gaps are zeroed;
+    deep_gemm.py, pre_permute_deepep_v2_to_deep_gemm: packed UE8M0 scales
+    need zero padding lanes)."""
     c = cases[name]
-    g, ref = c["g"], c["ref"]
-    lay = _gpu_layout(mx, c)
+    cfg, g, ref, inp = c["cfg"], c["g"], c["ref"], c["inp"]
+    M_cap, sl, nv = c["M_cap"], c["sl"], inp["n_valid"]
+    xe, xe_s, row_w = _poisoned_scatter_buffers(mx, M_cap, cfg.H, sl)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    xe, xe_s, row_w = mx.expand_scatter(g["x_q"], g["x_s"], c["sl"], g["topk_w"], lay,
-                                        n_valid=g["n_valid_dev"], status=status)
+    lay = _gpu_layout(mx, c)
+    mx.expand_scatter(g["x_q"], g["x_s"], sl, g["topk_w"], lay, n_valid=g["n_valid_dev"],
+                      xe=xe, xe_scale=xe_s, row_w=row_w, status=status)
     torch.cuda.synchronize()
     assert status.item() == 0
-    tot = ref["total"]
-    assert np.array_equal(xe.cpu().numpy()[:tot], ref["xe"][:tot])
-    assert np.array_equal(row_w.cpu().numpy().view(np.uint32)[:tot], ref["row_w"].view(np.uint32)[:tot])
-    xs = xe_s.cpu().numpy()
-    if c["sl"] == 0:
-        assert np.array_equal(xs[:tot].view(np.uint32), ref["xe_s"][:tot].view(np.uint32))
-    else:
-        assert np.array_equal(xs[:, :tot], ref["xe_s"][:, :tot])
+    _assert_scatter_equal(xe, xe_s, row_w, sl, ref["xe"], ref["xe_s"], ref["row_w"], ref["total"],
+                          f"{name} first routing")
+
+    ids2 = _rotated_routing(inp["topk_ids"], cfg.E)
+    rl2 = orc.layout(ids2, cfg.E, cfg.align, nv, M_cap)
+    assert rl2["rc"] == 0
+    rxe2, rxs2, rrw2 = orc.scatter(inp["x_q"], inp["x_s"], inp["scale_layout"], inp["topk_w"], rl2,
+                                   nv, cfg.E, cfg.align, M_cap)
+    tot2 = rl2["total"]
+    data1 = np.zeros(M_cap, bool)
+    data1[ref["layout"]["src2dst"][:nv][ref["layout"]["src2dst"][:nv] >= 0]] = True
+    gaps2 = np.ones(tot2, bool)
+    gaps2[rl2["src2dst"][:nv][rl2["src2dst"][:nv] >= 0]] = False
+    assert gaps2.sum() == 0 or (gaps2 & data1[:tot2]).any(), "no data row became a gap"
+    lay2 = mx.expand_layout(torch.from_numpy(ids2).cuda(), cfg.E, cfg.align, M_cap,
+                            n_valid=g["n_valid_dev"], status=status)
+    mx.expand_scatter(g["x_q"], g["x_s"], sl, g["topk_w"], lay2, n_valid=g["n_valid_dev"],
+                      xe=xe, xe_scale=xe_s, row_w=row_w, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    _assert_scatter_equal(xe, xe_s, row_w, sl, rxe2, rxs2, rrw2, tot2, f"{name} second routing")
 
 
 @pytest.mark.parametrize("name", NAMES)
@@ -142,7 +191,7 @@ MULTI_CHUNK = (
 def test_layout_scatter_multi_chunk_bit_exact(mx, orc, cfg, fused):
     """Layout and scatter over several chunks against the oracle, bit for
     bit, through moe_expand_layout + moe_expand_scatter and through
-    moe_expand_layout_scatter."""
+    moe_expand_layout_scatter, into buffers full of garbage."""
     d = synth.generate(cfg, device="cpu")
     inp = orc.to_numpy_inputs(d)
     M_cap = orc.expanded_capacity(cfg.T * cfg.K, cfg.E, cfg.align)
@@ -155,14 +204,15 @@ def test_layout_scatter_multi_chunk_bit_exact(mx, orc, cfg, fused):
     g = {k: v.cuda() for k, v in d.items() if isinstance(v, torch.Tensor)}
     nvd = torch.tensor([nv], dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    xe, xe_s, row_w = _poisoned_scatter_buffers(mx, M_cap, cfg.H, sl)
     if fused:
         lay, xe, xe_s, row_w = mx.expand_layout_scatter(
             g["x_q"], g["x_s"], sl, g["topk_ids"], g["topk_w"], cfg.E, cfg.align, M_cap,
-            n_valid=nvd, status=status)
+            n_valid=nvd, status=status, xe=xe, xe_scale=xe_s, row_w=row_w)
     else:
         lay = mx.expand_layout(g["topk_ids"], cfg.E, cfg.align, M_cap, n_valid=nvd, status=status)
-        xe, xe_s, row_w = mx.expand_scatter(g["x_q"], g["x_s"], sl, g["topk_w"], lay,
-                                            n_valid=nvd, status=status)
+        mx.expand_scatter(g["x_q"], g["x_s"], sl, g["topk_w"], lay, n_valid=nvd, xe=xe,
+                          xe_scale=xe_s, row_w=row_w, status=status)
     torch.cuda.synchronize()
     assert status.item() == 0
     tot = rl["total"]
@@ -592,4 +642,30 @@ def test_host_pipeline_matches_forward(mx, cases, mode):
     nv = c["inp"]["n_valid"]
     for k in range(len(batches)):
         assert torch.equal(outs[k][:nv], want[k][:nv]), k
+    assert layer.status.item() == 0
+
+
+@pytest.mark.parametrize("name", ["mid_padded", "mid_ue8m0_ragged"])
+def test_host_pipeline_copies_only_the_valid_prefix(mx, cases, name):
+    """HostPipeline.submit(..., n_rows=n) moves only rows [0, n) both ways
+    (column-major packed scales by word row) and gives the forward's output
+    on those rows; host rows past n are left as they were."""
+    c = cases[name]
+    cfg, g = c["cfg"], c["g"]
+    nv = min(c["inp"]["n_valid"], cfg.T - 37)
+    layer = _layer(mx, c)
+    nvd = torch.tensor([nv], dtype=torch.int32, device="cuda")
+    want = layer.forward(g["x_q"], g["x_s"], g["topk_ids"], g["topk_w"], nvd)[:nv].cpu().clone()
+    host = [t.cpu().pin_memory() for t in (g["x_q"], g["x_s"], g["topk_ids"], g["topk_w"])]
+    nv_h = torch.tensor([nv], dtype=torch.int32).pin_memory()
+    pipe = mx.HostPipeline(layer)
+    outs = []
+    for _ in range(3):
+        o = torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.bfloat16).pin_memory()
+        pipe.submit(*host, nv_h, o, n_rows=nv)
+        outs.append(o)
+    pipe.synchronize()
+    for o in outs:
+        assert torch.equal(o[:nv], want)
+        assert torch.isnan(o[nv:].float()).all()
     assert layer.status.item() == 0

@@ -72,6 +72,45 @@ def test_noalloc_layout_equals_the_allocating_call_twice_in_a_row(lib, names):
             assert np.array_equal(got[k], want[k]), (name, k)
 
 
+def _launch(lib, which, ids, E, align, n_valid, M_cap, o, ws=None):
+    T, K = ids.shape
+    s = torch.cuda.current_stream().cuda_stream
+    args = [ids.data_ptr(), T, K, E, align, n_valid.data_ptr(), M_cap, o["psum"].data_ptr(),
+            o["start"].data_ptr(), o["total"].data_ptr(), o["m_indices"].data_ptr(),
+            o["src2dst"].data_ptr(), o["tile_prefix"].data_ptr()]
+    if which == "noalloc":
+        rc = lib.moe_expand_layout_noalloc(*args, o["status"].data_ptr(), s)
+    else:
+        rc = lib.moe_expand_layout(*args, ws.data_ptr(), ws.numel(), o["status"].data_ptr(), s)
+    assert rc == 0, lib.moe_last_error_string()
+
+
+def test_noalloc_calls_queued_on_one_stream_without_a_host_wait(lib):
+    """The array is shared by every call, and the contract is stream order:
+    three calls with different inputs and separate outputs queued back to back
+    on one stream, with no synchronisation between them, each give what the
+    allocating call gives."""
+    dev = "cuda"
+    runs = []
+    for name in ("uniform_t4096_h4096", "zipf_t16384_h7168", "mid_zipf_ragged"):
+        cfg = synth.config_by_name(name)
+        d = synth.generate(cfg, device=dev, with_weights=False)
+        nv = torch.tensor([d["n_valid"]], dtype=torch.int32, device=dev)
+        M_cap = lib.moe_expanded_capacity(cfg.T, cfg.K, cfg.E, cfg.align)
+        runs.append((cfg, d["topk_ids"], nv, M_cap))
+    outs = []
+    for cfg, ids, nv, M_cap in runs:               # queued, no host wait in between
+        o = _outputs(cfg.T, cfg.K, cfg.E, M_cap, dev)
+        _launch(lib, "noalloc", ids, cfg.E, cfg.align, nv, M_cap, o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    for (cfg, ids, nv, M_cap), o in zip(runs, outs):
+        want = _run(lib, "ws", ids, cfg.E, cfg.align, nv, M_cap)
+        assert o["status"].item() == 0
+        for k in ("psum", "start", "total", "m_indices", "src2dst", "tile_prefix"):
+            assert np.array_equal(o[k].cpu().numpy(), want[k]), (cfg.name, k)
+
+
 def test_noalloc_refuses_sizes_beyond_its_scratch(lib):
     cap = lib.moe_expand_layout_noalloc_max_scratch()
     assert cap == 1 << 20
