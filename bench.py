@@ -78,8 +78,6 @@ def parse_args(argv=None):
                     help="run gate_up and act+quant as two launches")
     ap.add_argument("--gemm-tile-n128", action="store_true",
                     help="force 128-column GEMM tiles (tuning comparison)")
-    ap.add_argument("--gemm-cta-pair", action="store_true",
-                    help="256 x 256 GEMM tiles on CTA pairs (tuning comparison)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-workload lines of the other four workloads")
     ap.add_argument("--per-config-steps", type=int, default=10)
@@ -232,8 +230,7 @@ def make_step(args, cfg, layer, d, n_valid, mx, L, stream):
     lay = layer.lay
     ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
     x_q, x_s, ids, w = d["x_q"], d["x_s"], d["topk_ids"], d["topk_w"]
-    gflags = (mx.MOE_GEMM_TILE_N128 if args.gemm_tile_n128 else 0) | \
-        (mx.MOE_GEMM_CTA_PAIR if args.gemm_cta_pair else 0)
+    gflags = mx.MOE_GEMM_TILE_N128 if args.gemm_tile_n128 else 0
     # gate_up carries silu*mul, the quantiser and the fold in its epilogue
     fused = not args.unfused and gflags == 0
 

@@ -14,7 +14,7 @@ from typing import Optional
 import torch
 
 from . import _capi
-from ._capi import (MOE_BLOCK_M, MOE_FFN_UNFUSED, MOE_FOLD_WEIGHT_INTO_SCALE, MOE_GEMM_CTA_PAIR,
+from ._capi import (MOE_BLOCK_M, MOE_FFN_UNFUSED, MOE_FOLD_WEIGHT_INTO_SCALE,
                     MOE_GEMM_PER_KBLOCK_PROMOTION,
                     MOE_GEMM_TILE_N128,
                     MOE_SCALE_F32_ROWMAJOR, MOE_SCALE_UE8M0_PACKED_COLMAJOR,
@@ -27,7 +27,7 @@ __all__ = [
     "HostPipeline", "CapturedForward", "Layout",
     "MoEError",
     "MOE_SCALE_F32_ROWMAJOR", "MOE_SCALE_UE8M0_PACKED_COLMAJOR", "MOE_FOLD_WEIGHT_INTO_SCALE",
-    "MOE_WEIGHT_OUTPUT_ROWS", "MOE_GEMM_TILE_N128", "MOE_GEMM_CTA_PAIR",
+    "MOE_WEIGHT_OUTPUT_ROWS", "MOE_GEMM_TILE_N128",
     "MOE_GEMM_PER_KBLOCK_PROMOTION", "MOE_FFN_UNFUSED", "MOE_BLOCK_M",
     "scale_layout_of",
 ]

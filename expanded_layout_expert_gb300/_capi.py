@@ -25,7 +25,6 @@ MOE_SCALE_UE8M0_PACKED_COLMAJOR = 1
 MOE_FOLD_WEIGHT_INTO_SCALE = 1
 MOE_WEIGHT_OUTPUT_ROWS = 2
 MOE_GEMM_TILE_N128 = 16
-MOE_GEMM_CTA_PAIR = 32
 MOE_GEMM_PER_KBLOCK_PROMOTION = 64
 MOE_FFN_UNFUSED = 128
 

@@ -102,7 +102,9 @@ MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int3
 
 // Warp-collective form of mbar_wait: every lane of the warp calls it and all
 // lanes leave together, so the loop stays warp-uniform (no per-lane exits to
-// reconverge, no separate vote afterwards).
+// reconverge, no separate vote afterwards). Every lane tests the barrier:
+// measured on GB300, having lane 0 test it alone and pass the answer on by
+// shuffle made the GEMM epilogues 10-18 % slower.
 MOE_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status,
                             long long limit_cycles = kWaitLimitCycles) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
@@ -174,42 +176,9 @@ MOE_DEV void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t
 }
 
 // 32 TMEM lanes (one per thread of the warp) x 32 consecutive 32-bit
-// columns, followed by the wait for the load, in one statement so that no
-// use of the registers can be scheduled before the data has arrived.
-MOE_DEV void tc_ld32_wait(uint32_t taddr, uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
-      "[%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-        "=r"(v[31])
-      : "r"(taddr)
-      : "memory");
-}
-
-// Same, 16 consecutive columns.
-MOE_DEV void tc_ld16_wait(uint32_t taddr, uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-        "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr)
-      : "memory");
-}
-
-// Split form for software pipelining: tc_ld32 issues the load, tc_wait32
-// waits for every load this thread issued. The wait names the destination
-// registers as read-write operands, so no use of them can be scheduled before
-// it, and they stay reserved from the load to the wait.
+// columns, without waiting: the registers are valid only after a later
+// tcgen05.wait::ld (tc_wait64 / tc_regs_landed name them so that no use moves
+// above that wait).
 MOE_DEV void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -224,18 +193,6 @@ MOE_DEV void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[31])
       : "r"(taddr)
       : "memory");
-}
-
-MOE_DEV void tc_wait32(uint32_t (&v)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
-                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
-                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]),
-                 "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
-                 "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]),
-                 "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
-               :
-               : "memory");
 }
 
 // Waits for every TMEM load this thread issued; names two 32-register
@@ -363,94 +320,6 @@ MOE_DEV void tc_regs_landed(uint32_t (&v)[32]) {
 // ue8m0 exponent byte -> 2^(byte-127) as fp32 (byte 0 is the subnormal 2^-127).
 MOE_DEV float ue8m0_to_f32(uint32_t b) {
   return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
-}
-
-}  // namespace moe
-
-// ---------------------------------------------------------------- CTA pairs
-// Helpers for kernels launched with 2-CTA clusters whose tensor-core work is
-// issued by the even CTA for both (tcgen05 .cta_group::2).
-namespace moe {
-
-MOE_DEV uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-MOE_DEV void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Shared::cluster address of the variable at shared::cta address `a` in CTA
-// `rank` of this cluster.
-MOE_DEV uint32_t mapa_shared(uint32_t a, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  return r;
-}
-
-// Arrive on an mbarrier that may live in the peer CTA (shared::cluster address).
-MOE_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// 2-D tiled load into this CTA's shared memory whose completion is counted on
-// an mbarrier of either CTA of the pair (shared::cluster address).
-MOE_DEV void tma_load_2d_pair(void* dst, const CUtensorMap* tm, int32_t x, int32_t y,
-                              uint32_t bar_cluster_addr) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster_addr)
-      : "memory");
-}
-
-MOE_DEV void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(slot)),
-               "r"(ncols)
-               : "memory");
-}
-
-MOE_DEV void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-MOE_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-// D[both CTAs' TMEM] (+)= A[both CTAs' smem, split along M] *
-// B[both CTAs' smem, split along N]^T; fp8 operands, K = 32.
-MOE_DEV void tc_mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive once on the mbarrier at the same shared offset in every CTA of
-// `mask` when all tcgen05 operations issued before have completed.
-MOE_DEV void tc_commit_pair_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-MOE_DEV void tc_commit_pair(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
 }
 
 }  // namespace moe

@@ -604,339 +604,6 @@ __global__ void __launch_bounds__(Cfg<BN, Staged, Fused>::kThreads, 1)
 }
 
 
-// ---------------------------------------------------------------------------
-// CTA-pair variant for N % 256 == 0 (the default): a 2-CTA cluster computes
-// one 256-row x 256-column tile with tcgen05.mma.cta_group::2 (M = 256).
-// Each CTA loads its own 128 rows of A and its own half (128 rows) of the W
-// tile, so per K block each SM moves 32 KB through shared memory instead of
-// the 48 KB a single-CTA 128 x 256 tile needs, while the tensor-core work
-// per SM stays the same. The even CTA issues the MMAs for both; its commits
-// are multicast to both CTAs' barriers; the odd CTA's TMA loads complete on
-// the even CTA's barrier; both CTAs' epilogues report a drained accumulator
-// to the even CTA. Each CTA's epilogue promotes its own 128 rows x 256
-// columns out of its own TMEM exactly as in the single-CTA kernel.
-// ---------------------------------------------------------------------------
-#ifndef MOE_GEMM_PAIR_STAGES
-#define MOE_GEMM_PAIR_STAGES 6
-#endif
-
-struct PairCfg {
-  static constexpr int kStages = MOE_GEMM_PAIR_STAGES;
-  static constexpr int kABytes = BM * BK;        // this CTA's 128 rows of A
-  static constexpr int kBBytes = 128 * BK;       // this CTA's half of the W tile
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kEpiWarps = 8;
-  static constexpr int kFirstEpiWarp = 2;
-  static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
-  static constexpr int kTmemCols = 512;          // two 256-column accumulators
-  static constexpr int kNumBars = 2 * kStages + 5;
-  static constexpr int kBarOffset = kStages * kStageBytes;
-  static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
-  static constexpr int kTraceOffset = kMiscOffset + 16;
-  static constexpr int kTableOffset = kTraceOffset + kTraceWords * 8;
-  static constexpr int kSmemBytes = 1024 + kTableOffset + (3 * kMaxE + 2) * 4;
-};
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1)
-    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                             const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using C = PairCfg;
-  constexpr int BN = 256;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-  uint64_t* empty = full + C::kStages;
-  uint64_t* tfull = empty + C::kStages;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* mma_done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOffset);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOffset + 4);
-  unsigned long long* s_trace = reinterpret_cast<unsigned long long*>(smem + C::kTraceOffset);
-  int* s_tp = reinterpret_cast<int*>(smem + C::kTableOffset);  // 128-row tiles, E+1
-  int* s_start = s_tp + (p.E + 1);                              // E
-  int* s_tp2 = s_start + p.E;                                   // 256-row tiles, E+1
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  const int cid = static_cast<int>(blockIdx.x >> 1);
-  const int nclusters = static_cast<int>(gridDim.x >> 1);
-  const bool tracing = p.trace != nullptr;
-  const long long t_kernel0 = clock64();
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 2 * C::kEpiWarps);  // both CTAs' epilogue warps
-    }
-    mbar_init(mma_done, 1);
-    *abort_flag = 0;
-    for (int i = 0; i < kTraceWords; ++i) s_trace[i] = 0ull;
-    fence_mbar_init();
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(tmem_slot, C::kTmemCols);
-    tmem_relinquish_pair();
-  }
-  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_tp[i] = p.tile_prefix[i];
-  for (int i = threadIdx.x; i < p.E; i += blockDim.x) s_start[i] = p.start[i];
-  __syncthreads();
-  if (warp == 0) {
-    // pair tiles per expert: ceil(128-row tiles / 2), prefix-summed
-    int carry = 0;
-    if (lane == 0) s_tp2[0] = 0;
-    for (int base = 0; base < p.E; base += 32) {
-      const int e = base + lane;
-      const int v = (e < p.E) ? (s_tp[e + 1] - s_tp[e] + 1) / 2 : 0;
-      int incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (e < p.E) s_tp2[e + 1] = carry + incl;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  // Both CTAs' barriers are initialised and TMEM allocated before any
-  // cross-CTA traffic.
-  cluster_sync_all();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  int total = *p.d_total;
-  if (total > p.M_cap) total = static_cast<int>(p.M_cap);
-  const int num_n = p.N / BN;
-  const int num_tiles = s_tp2[p.E] * num_n;
-  const int KB = p.Kd / BK;
-  const int NB = p.N / 128;
-  const uint32_t full_lead = mapa_shared(smem_u32(&full[0]), 0);
-  const uint32_t tempty_lead = mapa_shared(smem_u32(&tempty[0]), 0);
-
-  // linear pair tile -> expert, first row of the 256-row tile, first row and
-  // row count of this CTA's half (the count can be <= 0 at a segment's end)
-  auto tile_rows = [&](int tile, int& e, int& row_me, int& rows_me) {
-    const int m = tile / num_n;
-    int lo = 0, hi = p.E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_tp2[mid] <= m) lo = mid; else hi = mid - 1;
-    }
-    e = lo;
-    row_me = s_start[e] + (m - s_tp2[e]) * 2 * BM + static_cast<int>(rank) * BM;
-    const int seg_end = (e + 1 < p.E) ? min(s_start[e + 1], total) : total;
-    rows_me = min(BM, seg_end - row_me);
-  };
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------------------------------------------------- producer
-      int stage = 0, issued = 0;
-      uint32_t phase = 0;
-      unsigned long long t_wait = 0;
-      for (int tile = cid; tile < num_tiles; tile += nclusters) {
-        int e, row_me, rows_me;
-        tile_rows(tile, e, row_me, rows_me);
-        const int n_me = (tile % num_n) * BN + static_cast<int>(rank) * 128;
-        bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
-          const long long t0 = tracing ? clock64() : 0;
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          if (tracing) t_wait += clock64() - t0;
-          uint8_t* sa = smem + stage * C::kStageBytes;
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
-          const uint32_t bar = full_lead + static_cast<uint32_t>(stage * 8);
-          tma_load_2d_pair(sa, &tmA, kb * BK, row_me, bar);
-          tma_load_2d_pair(sa + C::kABytes, &tmB, kb * BK, e * p.N + n_me, bar);
-          ++issued;
-          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-        }
-        if (!ok) break;
-      }
-      if (tracing) s_trace[kTrProdWait] = t_wait;
-      // The even CTA's full barriers count both CTAs' bytes: once they have
-      // completed, every load of the pair has landed.
-      if (leader) {
-        const int outstanding = issued < C::kStages ? issued : C::kStages;
-        for (int i = 1; i <= outstanding; ++i) {
-          int s = stage - i;
-          uint32_t ph = phase;
-          if (s < 0) { s += C::kStages; ph ^= 1u; }
-          drain_wait(&full[s], ph);
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && leader) {
-      // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_f8_f32(2 * BM, BN);
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      unsigned long long t_tmem = 0, t_data = 0, nkb = 0;
-      for (int tile = cid; tile < num_tiles; tile += nclusters) {
-        bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
-          const long long t0 = tracing ? clock64() : 0;
-          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          const long long t1 = tracing ? clock64() : 0;
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
-          if (tracing) {
-            const long long t2 = clock64();
-            t_tmem += t1 - t0;
-            t_data += t2 - t1;
-            ++nkb;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
-          const uint32_t sb = sa + C::kABytes;
-          const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
-#pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k)
-            tc_mma_f8_pair(d, sw128_kmajor_desc(sa + k * UMMA_K),
-                           sw128_kmajor_desc(sb + k * UMMA_K), idesc, k > 0 ? 1u : 0u);
-          tc_commit_pair_mc(&empty[stage], 0x3);
-          tc_commit_pair_mc(&tfull[acc], 0x3);
-          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1u;
-        }
-        if (!ok) break;
-      }
-      if (tracing) {
-        s_trace[kTrMmaWaitTmem] = t_tmem;
-        s_trace[kTrMmaWaitData] = t_data;
-        s_trace[kTrKBlocks] = nkb;
-      }
-      // Every MMA issued so far must complete before either CTA frees TMEM.
-      tc_commit_pair_mc(mma_done, 0x1);
-      drain_wait(mma_done, 0);
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int ew = warp - C::kFirstEpiWarp;
-    const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
-    const int half = ew >> 2;      // which 128-column half of the 256-column tile
-    const int row_in_tile = quarter * 32 + lane;
-    const uint8_t* ws8 = static_cast<const uint8_t*>(p.w_scale);
-    const float* wsf = static_cast<const float*>(p.w_scale);
-    const float* asf = static_cast<const float*>(p.a_scale);
-    const uint32_t* asw = static_cast<const uint32_t*>(p.a_scale);
-    int acc_buf = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int tile = cid; tile < num_tiles && ok; tile += nclusters) {
-      int e, row_me, rows_me;
-      tile_rows(tile, e, row_me, rows_me);
-      const int n_tile = tile % num_n;
-      const int nb = (n_tile * BN) / 128 + half;
-      const int row = row_me + row_in_tile;
-      const bool row_ok = row_in_tile < rows_me && row < p.M_cap;
-      const int64_t wbase = (static_cast<int64_t>(e) * NB + nb) * KB;
-
-      auto load_raw = [&](int kb, uint32_t& ra, uint32_t& rw) {
-        if (kb >= KB) {
-          ra = 0u;
-          rw = 0u;
-          return;
-        }
-        rw = p.ue8m0 ? static_cast<uint32_t>(ws8[wbase + kb]) : __float_as_uint(wsf[wbase + kb]);
-        ra = 0u;
-        if (row_ok)
-          ra = p.ue8m0 ? asw[static_cast<int64_t>(kb >> 2) * p.ld_as + row]
-                       : __float_as_uint(asf[static_cast<int64_t>(row) * p.ld_as + kb]);
-      };
-      auto decode = [&](int kb, uint32_t ra, uint32_t rw) -> float {
-        if (p.ue8m0) return ue8m0_to_f32((ra >> (8 * (kb & 3))) & 0xFFu) * ue8m0_to_f32(rw);
-        return __uint_as_float(ra) * __uint_as_float(rw);
-      };
-
-      float2 acc[64];
-#pragma unroll
-      for (int j = 0; j < 64; ++j) acc[j] = make_float2(0.0f, 0.0f);
-
-      auto kblock = [&](int kb, uint32_t& ra, uint32_t& rw) {
-        if (!ok || kb >= KB) return;
-        const float sc1 = decode(kb, ra, rw);
-        const float2 sc = make_float2(sc1, sc1);
-        load_raw(kb + 2, ra, rw);
-        const bool got = mbar_wait_warp(&tfull[acc_buf], acc_phase, abort_flag, p.status);
-        if (!got) {
-          ok = false;
-          return;
-        }
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                               static_cast<uint32_t>(acc_buf * BN + half * 128);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[16];
-          tc_ld16_wait(taddr + c * 16, v);
-          if (c == 7) {
-            // this accumulator is drained once every load from it has landed
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty_lead + static_cast<uint32_t>(acc_buf * 8));
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            acc[c * 8 + j] = __ffma2_rn(sc, make_float2(__uint_as_float(v[2 * j]),
-                                                        __uint_as_float(v[2 * j + 1])),
-                                        acc[c * 8 + j]);
-        }
-        acc_buf ^= 1;
-        if (acc_buf == 0) acc_phase ^= 1u;
-      };
-
-      uint32_t ra0, rw0, ra1, rw1;
-      load_raw(0, ra0, rw0);
-      load_raw(1, ra1, rw1);
-      for (int kb0 = 0; kb0 < KB && ok; kb0 += 2) {
-        kblock(kb0 + 0, ra0, rw0);
-        kblock(kb0 + 1, ra1, rw1);
-      }
-      if (!ok) break;
-      if (row_ok) {
-        const float wm = p.weight_rows ? p.row_w[row] : 1.0f;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.N +
-                                              n_tile * BN + half * 128);
-#pragma unroll
-        for (int v = 0; v < 16; ++v) {
-          uint4 o;
-          o.x = pack_bf16x2(acc[v * 4 + 0].x * wm, acc[v * 4 + 0].y * wm);
-          o.y = pack_bf16x2(acc[v * 4 + 1].x * wm, acc[v * 4 + 1].y * wm);
-          o.z = pack_bf16x2(acc[v * 4 + 2].x * wm, acc[v * 4 + 2].y * wm);
-          o.w = pack_bf16x2(acc[v * 4 + 3].x * wm, acc[v * 4 + 3].y * wm);
-          dst[v] = o;
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  // The even CTA's MMAs into this CTA's TMEM have all completed once the even
-  // CTA's MMA thread has drained; only then may either CTA free TMEM.
-  cluster_sync_all();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, C::kTmemCols);
-  }
-  if (tracing && threadIdx.x == 0) {
-    s_trace[kTrKernel] = static_cast<unsigned long long>(clock64() - t_kernel0);
-    for (int i = 0; i < kTraceWords; ++i) p.trace[blockIdx.x * kTraceWords + i] = s_trace[i];
-  }
-}
-
 std::atomic<unsigned long long*> g_trace{nullptr};
 
 template <int BN, bool Staged, bool Fused, bool Ue8m0>
@@ -960,21 +627,6 @@ template <int BN, bool Staged, bool Fused = false>
 int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm, cudaStream_t s) {
   return prm.ue8m0 ? launch_fmt<BN, Staged, Fused, true>(ta, tb, prm, s)
                    : launch_fmt<BN, Staged, Fused, false>(ta, tb, prm, s);
-}
-
-int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm, cudaStream_t s) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(grouped_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PairCfg::kSmemBytes) != cudaSuccess)
-      return check_launch("cudaFuncSetAttribute(grouped_gemm_pair_kernel)");
-    attr_set[dev] = true;
-  }
-  const int grid = device_sm_count() & ~1;  // whole CTA pairs
-  grouped_gemm_pair_kernel<<<grid, PairCfg::kThreads, PairCfg::kSmemBytes, s>>>(ta, tb, prm);
-  return check_launch("grouped_gemm_pair_kernel");
 }
 
 }  // namespace
@@ -1012,8 +664,7 @@ extern "C" int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale
 
   // Power-of-two scales go to the tensor core's block scaling.
   const bool block_scaled = scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR && N % 256 == 0 &&
-                            !(flags & (MOE_GEMM_TILE_N128 | MOE_GEMM_CTA_PAIR |
-                                       MOE_GEMM_PER_KBLOCK_PROMOTION));
+                            !(flags & (MOE_GEMM_TILE_N128 | MOE_GEMM_PER_KBLOCK_PROMOTION));
   if (block_scaled) {
     moe::MxGemmArgs a;
     a.A = A;
@@ -1034,12 +685,11 @@ extern "C" int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale
     a.trace = moe::g_trace.load();
     return moe::launch_grouped_gemm_mx(a, reinterpret_cast<cudaStream_t>(stream));
   }
-  const bool pair = N % 256 == 0 && (flags & MOE_GEMM_CTA_PAIR) && !(flags & MOE_GEMM_TILE_N128);
   const int BN = (N % 256 == 0 && !(flags & MOE_GEMM_TILE_N128)) ? 256 : 128;
   CUtensorMap ta, tb;
   int rc = moe::make_tmap_k128(&ta, A, Kd, M_cap, Kd, moe::BM);
   if (rc != MOE_OK) return rc;
-  rc = moe::make_tmap_k128(&tb, W, Kd, static_cast<uint64_t>(E) * N, Kd, pair ? 128 : BN);
+  rc = moe::make_tmap_k128(&tb, W, Kd, static_cast<uint64_t>(E) * N, Kd, BN);
   if (rc != MOE_OK) return rc;
   moe::Params prm;
   prm.a_scale = A_scale;
@@ -1061,7 +711,6 @@ extern "C" int moe_grouped_gemm(const uint8_t* A, const void* A_scale, int scale
   prm.di_scale = nullptr;
   prm.ld_ds = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (pair) return moe::launch_pair(ta, tb, prm, s);
   // Short-K GEMMs (down_proj) spend a larger share of each tile on the
   // store, so they take the staged store; long-K ones keep the L1 room.
   const bool staged = (Kd / 128) <= MOE_GEMM_STAGED_MAX_KB;

@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(tfull, 1);
     mbar_init(tempty, kEpiWarps);
     mbar_init(mma_done, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(&amax_bar[q], 64);  // both warps of the quarter
+    for (int q = 0; q < 4; ++q) mbar_init(&amax_bar[q], 2);  // lane 0 of both warps of the quarter
     *abort_flag = 0;
     for (int i = 0; i < kTraceWords; ++i) s_trace[i] = 0ull;
     fence_mbar_init();
@@ -411,10 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the other half's maximum for the same row (double-buffered by tile)
         const int par = iter & 1;
         s_amax[(par * 2 + half) * 128 + row_in_tile] = m;
-        mbar_arrive(&amax_bar[quarter]);
-        const bool got2 = mbar_wait(&amax_bar[quarter], static_cast<uint32_t>(par), abort_flag,
-                                    p.status);
-        if (!__all_sync(0xffffffffu, got2)) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&amax_bar[quarter]);
+        const bool got2 = mbar_wait_warp(&amax_bar[quarter], static_cast<uint32_t>(par),
+                                         abort_flag, p.status);
+        if (!got2) break;
         const float amax = fmaxf(m, s_amax[(par * 2 + (half ^ 1)) * 128 + row_in_tile]);
         float sc, inv;
         uint32_t b;

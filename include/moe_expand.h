@@ -67,7 +67,6 @@ typedef struct CUstream_st* moe_stream_t; /* the same type as cudaStream_t */
 #define MOE_FOLD_WEIGHT_INTO_SCALE 1 /* fp32 path: store s*w as down_proj's input scale */
 #define MOE_WEIGHT_OUTPUT_ROWS     2 /* ue8m0 path: multiply the down_proj output row by w */
 #define MOE_GEMM_TILE_N128        16 /* tuning: use 128-column GEMM tiles even when N % 256 == 0 */
-#define MOE_GEMM_CTA_PAIR         32 /* tuning: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2) */
 #define MOE_GEMM_PER_KBLOCK_PROMOTION 64 /* ue8m0 scales: promote per K block in registers instead of
                                             the tensor core's block scaling */
 #define MOE_FFN_UNFUSED          128 /* moe_grouped_ffn: gate_up, act+quant and down as three launches */
