@@ -71,9 +71,9 @@ def parse_args(argv=None):
                     help="decode variant: both GEMMs on per-expert slabs of this height")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of a CUDA graph of the whole forward (no per-kernel split)")
-    ap.add_argument("--fuse-layout-scatter", action="store_true",
-                    help="layout and expand-scatter as one call of two launches "
-                         "(moe_expand_layout_scatter)")
+    ap.add_argument("--fuse-layout-scatter", action=argparse.BooleanOptionalAction, default=True,
+                    help="layout and expand-scatter as one moe_expand_layout_scatter call "
+                         "(one cooperative launch); --no-fuse-layout-scatter: two calls")
     ap.add_argument("--unfused", action="store_true",
                     help="run gate_up and act+quant as two launches")
     ap.add_argument("--gemm-tile-n128", action="store_true",
@@ -209,13 +209,37 @@ def algorithmic_work(cfg, P: int, M_pad: int, nv: int):
 
 # ------------------------------------------------------------------ our arm
 
-def launches_per_step(args, cfg, fused: bool) -> int:
-    """Kernels one step launches: layout 2 (1 when all pairs fit one
-    2048-pair chunk) + scatter 1, or 2 for the fused layout+scatter call;
-    gate_up (with act+quant when fused, else + act_quant 1); down 1 (the
-    masked slab adds its two bridges); combine 1."""
-    one_chunk = cfg.T * cfg.K <= 2048
-    front = 2 if args.fuse_layout_scatter else (2 if one_chunk else 3)
+def coop_blocks_per_sm(E: int, scatter: bool) -> int:
+    """Resident blocks per SM of the cooperative layout kernel: 3 (40
+    registers x 512 threads), 2 for the variant fused with the scatter (64
+    registers), fewer when its 19*E ints of shared memory per block do not
+    fit the SM's 228 KB (1 KB reserved per block)."""
+    by_smem = (228 * 1024) // (19 * 4 * E + 1024 + 64)
+    return max(0, min(2 if scatter else 3, by_smem))
+
+
+def front_launches(T: int, K: int, E: int, H: int, fuse: bool, sms: int) -> int:
+    """Kernels the layout and the expand-scatter launch. moe_expand_layout:
+    1 (one block when all pairs fit one 2048-pair chunk; one cooperative
+    launch when the grid holds every chunk), else 2. The scatter: 1. The
+    fused call: 1 cooperative launch for 2+ chunks when its grid holds
+    every chunk and the copy's 32-bit work counter suffices, else the two
+    calls."""
+    nb = max(1, -(-T * K // 2048))
+    layout = 1 if nb == 1 or nb <= coop_blocks_per_sm(E, False) * sms else 2
+    if fuse and nb > 1:
+        cap = coop_blocks_per_sm(E, True) * sms
+        nseg = -(-(H // 16) // 64)
+        if nb <= cap and T * nseg + cap * 16 * 4 <= 2**32 - 1:
+            return 1
+    return layout + 1
+
+
+def launches_per_step(args, cfg, fused: bool, sms: int) -> int:
+    """Kernels one step launches: layout + scatter (front_launches); gate_up
+    (with act+quant when fused, else + act_quant 1); down 1 (the masked slab
+    adds its two bridges); combine 1."""
+    front = front_launches(cfg.T, cfg.K, cfg.E, cfg.H, args.fuse_layout_scatter, sms)
     ffn = 4 if args.masked_max_m else (2 if fused else 3)
     return front + ffn + 1
 
@@ -366,14 +390,17 @@ def kernel_split(per_kernel_ms, work, fused, args, hbm, fp8_peak):
         if args.fuse_layout_scatter and n == "layout":
             kernels[n] = {"ms": 0.0, "fused_into": "scatter"}
             continue
+        w = work[n]
+        if args.fuse_layout_scatter and n == "scatter":
+            w = work["scatter"] + work["layout"]  # one call moves both
         if n.startswith("gemm"):
             ach = work[n] / (ms / 1e3) / 1e12
             kernels[n] = {"ms": round(ms, 4), "ms_median": round(med, 4), "achieved": round(ach, 1),
                           "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4), "work": work[n]}
         else:
-            ach = work[n] / (ms / 1e3) / 1e9
+            ach = w / (ms / 1e3) / 1e9
             kernels[n] = {"ms": round(ms, 4), "ms_median": round(med, 4), "achieved": round(ach, 1),
-                          "unit": "GB/s", "frac": round(ach / hbm, 4), "work": work[n]}
+                          "unit": "GB/s", "frac": round(ach / hbm, 4), "work": w}
     return kernels
 
 
@@ -469,7 +496,7 @@ def run_ours(args, world, rank, local):
     else:
         kernels = kernel_split(per_kernel, work, fused, args, hbm, fp8_peak)
         pk = {n: statistics.mean(v) for n, v in per_kernel.items()}
-        sc_bytes = work["scatter"] + work["combine"]
+        sc_bytes = work["scatter"] + work["combine"] + (work["layout"] if args.fuse_layout_scatter else 0)
         sc_gbs = sc_bytes / ((pk["scatter"] + pk["combine"]) / 1e3) / 1e9
         gemm_tflops = (work["gemm1"] + work["gemm2"]) / ((pk["gemm1"] + pk["gemm2"]) / 1e3) / 1e12
         roofline = {"bound": "tensor",
@@ -490,7 +517,8 @@ def run_ours(args, world, rank, local):
         "grouped_fp8_tflops": None if args.graph else round(gemm_tflops, 1),
         "kernels": kernels,
         "roofline": roofline,
-        "gpu_launches": launches_per_step(args, cfg, fused) * args.steps,
+        "gpu_launches": launches_per_step(
+            args, cfg, fused, torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": round(t_wall, 3),
     }
@@ -526,7 +554,8 @@ def workload_config(cfg, nv, P, M_pad, layer, args, world):
             "weighting": args.weighting,
             "masked_max_m": args.masked_max_m or None,
             "cuda_graph": bool(args.graph),
-            "layout_scatter": "one call, 2 launches" if args.fuse_layout_scatter else "2 calls",
+            "layout_scatter": ("one call (moe_expand_layout_scatter)" if args.fuse_layout_scatter
+                               else "2 calls"),
             "valid_pairs": P, "expanded_rows": M_pad, "M_cap": layer.M_cap,
             "l2": "flushed between steps (256 MiB write outside the timed events)",
             "parallelism": f"replicas x{world} (token-sharded, no collective)"}

@@ -135,9 +135,10 @@ def expand_layout_scatter(x_q: torch.Tensor, x_scale: torch.Tensor, scale_layout
                           out: Optional[Layout] = None, xe: Optional[torch.Tensor] = None,
                           xe_scale: Optional[torch.Tensor] = None,
                           row_w: Optional[torch.Tensor] = None, stream=None):
-    """The layout and the expand-scatter in two launches (the layout's
-    count/scan, then rank + copy per chunk); same outputs as expand_layout
-    followed by expand_scatter. Returns (layout, xe, xe_scale, row_w)."""
+    """The layout and the expand-scatter in one call (one cooperative
+    launch when the grid holds every 2048-pair chunk); same outputs as
+    expand_layout followed by expand_scatter. Returns (layout, xe, xe_scale,
+    row_w)."""
     T, H = x_q.shape
     K = topk_ids.shape[1]
     dev = x_q.device
@@ -277,15 +278,16 @@ class ExpandedMoELayer:
     / moe_masked_slab_to_expand); the weight multiplies each pair's down row
     on the way back (no fold); an expert with more rows than masked_max_m
     drops the extra ones and flags the status word.
-    fuse_layout_scatter: run the layout and the expand-scatter as
-    moe_expand_layout_scatter (two launches: count/scan, then rank + copy per
-    chunk) instead of moe_expand_layout + moe_expand_scatter (three); the
-    outputs are the same bit for bit.
+    fuse_layout_scatter (default True): run the layout and the
+    expand-scatter as one moe_expand_layout_scatter call (one cooperative
+    launch when the grid holds every 2048-pair chunk) instead of
+    moe_expand_layout + moe_expand_scatter; the outputs are the same bit for
+    bit.
     """
 
     def __init__(self, w13, s13, w2, s2, *, K: int, align: int, scale_mode: str,
                  max_tokens: int, device=None, weighting: str = "expanded",
-                 masked_max_m: Optional[int] = None, fuse_layout_scatter: bool = False):
+                 masked_max_m: Optional[int] = None, fuse_layout_scatter: bool = True):
         self.w13, self.s13, self.w2, self.s2 = w13, s13, w2, s2
         self.E, twoI, self.H = w13.shape
         self.I = twoI // 2
@@ -440,9 +442,9 @@ class ExpandedMoELayer:
                                        device=self.device)
         return self._gateup
 
-    # kernels one forward launches: layout 2 (1 when all pairs fit one
-    # 2048-pair chunk), scatter 1, gate_up with act+quant fused 1, down 1,
-    # combine 1; with fuse_layout_scatter, layout + scatter take 2
+    # kernels one forward launches at most: layout + scatter 3 (1 when the
+    # cooperative grid holds every 2048-pair chunk), gate_up with act+quant
+    # fused 1, down 1, combine 1
     KERNELS_PER_FORWARD = 6
 
 

@@ -375,6 +375,503 @@ __global__ void __launch_bounds__(kThreads) layout_single_kernel(
 }  // namespace
 }  // namespace moe
 
+// ---------------------------------------------------------------------------
+// The layout (and the layout fused with the expand-scatter) in ONE launch.
+// A cooperative launch puts every block on the GPU at once, so blocks may
+// wait for each other at a grid-wide barrier (bounded, like every wait in
+// this library). Blocks 0 .. nb-1 own one 2048-pair chunk each (16 warps):
+//   A. each warp ranks its 128 pairs among themselves (match_any groups
+//      the lanes holding one expert; the lowest lane advances the warp's
+//      counter), then the block turns the per-warp counts into per-warp
+//      offsets and publishes the chunk's count per expert;
+//   -- barrier of the chunk blocks --
+//   C. every chunk block reads the whole count table (E x chunks, from L2,
+//      a group of lanes per expert) and derives the expert totals, the
+//      aligned segment starts (one warp scans the experts) and its own
+//      chunk's first row per expert;
+//   D. it writes src2dst of its chunk: segment start + earlier chunks +
+//      earlier warps + the rank inside the warp;
+//   E. the chunk blocks label m_indices, four consecutive rows per thread
+//      and one search per four rows.
+// Fused with the scatter, the grid has more blocks than chunks; the others
+// go straight to the second barrier, which all blocks meet:
+//   -- barrier of all blocks --
+//   F. the whole grid zeroes the alignment gaps, then copies every valid
+//      token's row, scale row and weight to its expanded rows. The copy's
+//      work items are 1 KB pieces of a token's row; warps take them from a
+//      shared counter, kCopyGrab at a time, so the grid finishes together.
+// The outputs equal those of the two-launch layout (and of
+// moe_expand_scatter) bit for bit. The four barrier and counter words live
+// in the workspace's ticket slot; the last block to leave resets them.
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+constexpr int kCoopThreads = 512;
+constexpr int kCoopWarps = kCoopThreads / 32;
+constexpr int kCoopPairsPerWarp = kChunk / kCoopWarps;  // 128
+constexpr int kCoopRounds = kCoopPairsPerWarp / 32;     // 4
+constexpr int kCoopMaxK = 32;
+constexpr int kCoopPadRows = 8;        // gap rows per work item of the copy phase
+constexpr int kCopyU = 2;              // 16-byte vectors per lane in flight in the copy
+constexpr int kCopyPiece = 32 * kCopyU;  // vectors per work item of the copy
+constexpr int kCopyGrab = 4;           // work items a warp takes per counter update
+// Words of the 256-byte ticket slot: barrier 1 (also the two-launch path's
+// ticket) and the exit count share the first 128-byte line; barrier 2 and
+// the copy's work counter are in the second, so blocks polling barrier 2
+// do not slow the traffic on barrier 1.
+constexpr int kBar1Word = 0, kExitWord = 8, kBar2Word = 32, kWorkWord = 48;
+constexpr size_t kSyncSlotBytes = 256;
+
+MOE_DEV unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of a cooperative launch: every block arrives once
+// (after its writes, released to the GPU), thread 0 waits until `target`
+// arrivals in all, sleeping sleep_ns between polls. Gives up after
+// kWaitLimitCycles with MOE_ERR_TIMEOUT; returns false then.
+MOE_DEV bool grid_sync(unsigned* arrivals, unsigned target, int32_t* status, int* s_flag,
+                       unsigned sleep_ns) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" : : "l"(arrivals) : "memory");
+    int ok = 1;
+    const long long t0 = clock64();
+    while (ld_acquire_u32(arrivals) < target) {
+      if (sleep_ns) __nanosleep(sleep_ns);
+      if (clock64() - t0 > kWaitLimitCycles) {
+        set_status(status, MOE_ERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+    }
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+// m_indices rows [r, r + 4) for r = first, first + stride, ...: e on
+// [start[e], start[e] + align(count_e)), -1 past the total; one search per
+// four rows.
+MOE_DEV void label_rows(int32_t* m_indices, int64_t M_cap, int total, const int* s_start, int E,
+                        int64_t first, int64_t stride) {
+  for (int64_t r0 = first; r0 < M_cap; r0 += stride) {
+    int e = 0;
+    if (r0 < total) {
+      int lo = 0, hi = E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_start[mid] <= r0) lo = mid; else hi = mid - 1;
+      }
+      e = lo;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t row = r0 + i;
+      if (row >= M_cap) break;
+      if (row < total) {
+        while (e + 1 < E && s_start[e + 1] <= row) ++e;
+        m_indices[row] = e;
+      } else {
+        m_indices[row] = -1;
+      }
+    }
+  }
+}
+
+struct CoopScatterArgs {
+  const float* topk_w;
+  const uint4* x;
+  const void* x_scale;
+  int ue8m0;
+  int64_t ld_xs;
+  int H;
+  uint4* xe;
+  void* xe_scale;
+  int64_t ld_xes;
+  float* row_w;
+};
+
+template <bool kScatter>
+__global__ void __launch_bounds__(kCoopThreads, kScatter ? 2 : 3) layout_coop_kernel(
+    const int32_t* __restrict__ ids, int64_t T, int K, int E, int align,
+    const int32_t* __restrict__ d_n_valid, int64_t M_cap, int nb, int32_t* __restrict__ counts,
+    unsigned* __restrict__ sync_words, int32_t* __restrict__ psum, int32_t* __restrict__ start,
+    int32_t* __restrict__ d_total, int32_t* __restrict__ tile_prefix,
+    int32_t* __restrict__ m_indices, int32_t* __restrict__ src2dst, int32_t* __restrict__ status,
+    const CoopScatterArgs sa) {
+  extern __shared__ int dyn[];
+  int* hist = dyn;                 // [E] expert totals
+  int* s_start = hist + E;         // [E] segment starts
+  int* s_base = s_start + E;       // [E] this chunk's first row per expert
+  int* wcnt = s_base + E;          // [kCoopWarps][E] per-warp counts, then offsets
+  __shared__ int s_flag, s_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = static_cast<int>(blockIdx.x);
+  const int64_t nv = valid_rows(d_n_valid, T);
+  unsigned* bar1 = sync_words + kBar1Word;
+  unsigned* exits = sync_words + kExitWord;
+  bool ok = true;
+
+  if (b < nb) {  // block-uniform: a chunk block
+    const int64_t all_pairs = T * K;
+    const int64_t npairs = nv * K;
+    const unsigned lt_mask = (1u << lane) - 1u;
+
+    // A: ranks inside each warp, per-warp offsets, the chunk's counts
+    for (int i = tid; i < kCoopWarps * E; i += kCoopThreads) wcnt[i] = 0;
+    __syncthreads();
+    const int64_t base_p = static_cast<int64_t>(b) * kChunk + warp * kCoopPairsPerWarp;
+    // per pair: expert << 8 | rank inside the warp (< 128), or -1
+    int rk[kCoopRounds];
+#pragma unroll
+    for (int j = 0; j < kCoopRounds; ++j) {
+      const int64_t p = base_p + j * 32 + lane;
+      rk[j] = p < npairs ? ids[p] : -1;
+    }
+    int* my = wcnt + warp * E;
+#pragma unroll
+    for (int j = 0; j < kCoopRounds; ++j) {
+      const int id = rk[j];
+      if (id >= E) set_status(status, MOE_ERR_DEVICE_CHECK);
+      const bool valid = (id >= 0 && id < E);
+      const int key = valid ? id : (E + static_cast<int>(lane));
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      rk[j] = valid ? (id << 8) | (my[id] + __popc(peers & lt_mask)) : -1;
+      __syncwarp();
+      if (valid && (peers & lt_mask) == 0u) my[id] += __popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kCoopThreads) {
+      int acc = 0;
+#pragma unroll
+      for (int w = 0; w < kCoopWarps; ++w) {
+        const int c = wcnt[w * E + e];
+        wcnt[w * E + e] = acc;
+        acc += c;
+      }
+      counts[static_cast<int64_t>(e) * nb + b] = acc;
+    }
+
+    ok = grid_sync(bar1, nb, status, &s_flag, 0);
+    if (ok) {
+      // C: per expert the total and the count of the chunks before this
+      // one; gsz lanes (a power of two) share an expert
+      int gsz = 32;
+      while (gsz > 1 && gsz * E > kCoopThreads) gsz >>= 1;
+      const int ngroups = kCoopThreads / gsz;
+      const int gl = tid & (gsz - 1);
+      for (int e0 = 0; e0 < E; e0 += ngroups) {  // uniform trip count
+        const int e = e0 + tid / gsz;
+        int tot = 0, pre = 0;
+        if (e < E) {
+          const int32_t* row = counts + static_cast<int64_t>(e) * nb;
+          for (int c = gl; c < nb; c += 4 * gsz) {
+            int v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int cc = c + u * gsz;
+              v[u] = cc < nb ? __ldcg(row + cc) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              tot += v[u];
+              if (c + u * gsz < b) pre += v[u];
+            }
+          }
+        }
+        for (int o = gsz >> 1; o > 0; o >>= 1) {
+          tot += __shfl_xor_sync(0xffffffffu, tot, o);
+          pre += __shfl_xor_sync(0xffffffffu, pre, o);
+        }
+        if (e < E && gl == 0) {
+          hist[e] = tot;
+          s_base[e] = pre;
+        }
+      }
+      __syncthreads();
+      // segment starts and tile prefix: warp 0 scans the experts, each lane
+      // a contiguous run of them
+      if (warp == 0) {
+        const int per = (E + 31) / 32;
+        const int e_lo = min(E, lane * per), e_hi = min(E, e_lo + per);
+        int rows = 0, tiles = 0;
+        for (int e = e_lo; e < e_hi; ++e) {
+          const int seg = align_up(hist[e], align);
+          rows += seg;
+          tiles += (seg + MOE_BLOCK_M - 1) / MOE_BLOCK_M;
+        }
+        int ir = rows, it = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int yr = __shfl_up_sync(0xffffffffu, ir, o);
+          const int yt = __shfl_up_sync(0xffffffffu, it, o);
+          if (lane >= o) {
+            ir += yr;
+            it += yt;
+          }
+        }
+        const int rows_total = __shfl_sync(0xffffffffu, ir, 31);
+        const int tiles_total = __shfl_sync(0xffffffffu, it, 31);
+        int run = ir - rows, trun = it - tiles;
+        for (int e = e_lo; e < e_hi; ++e) {
+          const int c = hist[e];
+          const int seg = align_up(c, align);
+          s_start[e] = run;
+          s_base[e] += run;
+          if (b == 0) {
+            start[e] = run;
+            psum[e] = run + c;
+            tile_prefix[e] = trun;
+          }
+          run += seg;
+          trun += (seg + MOE_BLOCK_M - 1) / MOE_BLOCK_M;
+        }
+        if (lane == 0) {
+          s_total = rows_total;
+          if (b == 0) {
+            tile_prefix[E] = tiles_total;
+            *d_total = rows_total;
+            if (rows_total > M_cap) set_status(status, MOE_ERR_DEVICE_CHECK);
+          }
+        }
+      }
+      __syncthreads();
+
+      // D: src2dst of this chunk's pairs
+#pragma unroll
+      for (int j = 0; j < kCoopRounds; ++j) {
+        const int64_t p = base_p + j * 32 + lane;
+        int dst = -1;
+        if (rk[j] >= 0) {
+          const int id = rk[j] >> 8;
+          dst = s_base[id] + my[id] + (rk[j] & 0xff);
+        }
+        if (p < all_pairs) src2dst[p] = (dst >= 0 && dst < M_cap) ? dst : -1;
+      }
+
+      // E: row labels (the fused kernel labels them after its second
+      // barrier, with the whole grid)
+      if (!kScatter)
+        label_rows(m_indices, M_cap, s_total, s_start, E,
+                   (static_cast<int64_t>(b) * kCoopThreads + tid) * 4,
+                   static_cast<int64_t>(nb) * kCoopThreads * 4);
+    }
+  }
+
+  if constexpr (kScatter) {
+    unsigned* bar2 = sync_words + kBar2Word;
+    unsigned* work = sync_words + kWorkWord;
+    if (ok) ok = grid_sync(bar2, gridDim.x, status, &s_flag, 128);
+    if (ok) {
+      // E: row labels from the published segment starts
+      for (int e = tid; e < E; e += kCoopThreads) s_start[e] = __ldcg(&start[e]);
+      if (tid == 0) s_total = __ldcg(d_total);
+      __syncthreads();
+      label_rows(m_indices, M_cap, s_total, s_start, E,
+                 (static_cast<int64_t>(b) * kCoopThreads + tid) * 4,
+                 static_cast<int64_t>(gridDim.x) * kCoopThreads * 4);
+      const int H = sa.H;
+      const int nvec = H / 16;
+      const int G = H / 128;
+      const int W = (G + 3) / 4;
+      // F1: alignment gaps [psum[e], align(psum[e])), 8 rows per work item
+      const int per_e = (align - 1 + kCoopPadRows - 1) / kCoopPadRows;
+      const int items = E * per_e;
+      for (int it = b; it < items; it += gridDim.x) {
+        const int e = it / per_e, sub = it % per_e;
+        const int pe = __ldcg(&psum[e]);
+        const int64_t seg_end = align_up(pe, align);
+        const int64_t r0 = static_cast<int64_t>(pe) + static_cast<int64_t>(sub) * kCoopPadRows;
+        int64_t r1 = r0 + kCoopPadRows;
+        if (r1 > seg_end) r1 = seg_end;
+        if (r1 > M_cap) r1 = M_cap;
+        for (int64_t r = r0; r < r1; ++r) {
+          for (int v = tid; v < nvec; v += kCoopThreads) sa.xe[r * nvec + v] = make_uint4(0, 0, 0, 0);
+          if (!sa.ue8m0) {
+            for (int g = tid; g < G; g += kCoopThreads)
+              static_cast<float*>(sa.xe_scale)[r * sa.ld_xes + g] = 0.0f;
+          } else {
+            for (int j = tid; j < W; j += kCoopThreads)
+              static_cast<int32_t*>(sa.xe_scale)[j * sa.ld_xes + r] = 0;
+          }
+          if (tid == 0) sa.row_w[r] = 0.0f;
+        }
+      }
+      // F2: work items (token, piece of kCopyPiece vectors) from the shared
+      // counter. Lane k < K holds pair k's row; every lane loads kCopyU
+      // vectors of the piece before storing them to the K rows. The first
+      // piece of a token also copies its scales and weights.
+      const int nseg = (nvec + kCopyPiece - 1) / kCopyPiece;
+      const int64_t n_items = nv * nseg;
+      for (;;) {
+        unsigned grab = 0;  // the host keeps the counter's range inside 32 bits
+        if (lane == 0) grab = atomicAdd(work, static_cast<unsigned>(kCopyGrab));
+        grab = __shfl_sync(0xffffffffu, grab, 0);
+        if (static_cast<int64_t>(grab) >= n_items) break;
+        const int64_t it_end = min(n_items, static_cast<int64_t>(grab) + kCopyGrab);
+        for (int64_t it = static_cast<int64_t>(grab); it < it_end; ++it) {
+          const int64_t t = it / nseg;
+          const int v0 = static_cast<int>(it - t * nseg) * kCopyPiece;
+          int r = -1;
+          if (lane < K) {
+            r = __ldcg(&src2dst[t * K + lane]);
+            if (r >= M_cap) {
+              set_status(status, MOE_ERR_DEVICE_CHECK);
+              r = -1;
+            }
+          }
+          const uint4* src = sa.x + t * nvec;
+          uint4 val[kCopyU];
+#pragma unroll
+          for (int u = 0; u < kCopyU; ++u) {
+            const int v = v0 + u * 32 + lane;
+            if (v < nvec) val[u] = __ldcs(src + v);
+          }
+          for (int k = 0; k < K; ++k) {
+            const int rk = __shfl_sync(0xffffffffu, r, k);
+            if (rk < 0) continue;
+            uint4* dst = sa.xe + static_cast<int64_t>(rk) * nvec;
+#pragma unroll
+            for (int u = 0; u < kCopyU; ++u) {
+              const int v = v0 + u * 32 + lane;
+              if (v < nvec) dst[v] = val[u];
+            }
+          }
+          if (v0 != 0) continue;
+          if (!sa.ue8m0) {
+            const float* xs = static_cast<const float*>(sa.x_scale);
+            float* ys = static_cast<float*>(sa.xe_scale);
+            for (int c0 = 0; c0 < G; c0 += 32) {
+              const int c = c0 + lane;
+              const float sv = c < G ? xs[t * sa.ld_xs + c] : 0.0f;
+              for (int k = 0; k < K; ++k) {
+                const int rk = __shfl_sync(0xffffffffu, r, k);
+                if (rk >= 0 && c < G) ys[static_cast<int64_t>(rk) * sa.ld_xes + c] = sv;
+              }
+            }
+          } else {
+            const int32_t* xs = static_cast<const int32_t*>(sa.x_scale);
+            int32_t* ys = static_cast<int32_t*>(sa.xe_scale);
+            for (int j0 = 0; j0 < W; j0 += 32) {
+              const int j = j0 + lane;
+              const int32_t wv = j < W ? xs[j * sa.ld_xs + t] : 0;
+              for (int k = 0; k < K; ++k) {
+                const int rk = __shfl_sync(0xffffffffu, r, k);
+                if (rk >= 0 && j < W) ys[j * sa.ld_xes + rk] = wv;
+              }
+            }
+          }
+          if (r >= 0) sa.row_w[r] = sa.topk_w[t * K + lane];
+        }
+      }
+    }
+  }
+
+  // the last block to leave makes the barrier and counter words ready for
+  // the next call
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(exits, 1u) == gridDim.x - 1) {
+      atomicExch(bar1, 0u);
+      atomicExch(exits, 0u);
+      atomicExch(sync_words + kBar2Word, 0u);
+      atomicExch(sync_words + kWorkWord, 0u);
+    }
+  }
+}
+
+size_t coop_smem_bytes(int E) {
+  return static_cast<size_t>(3 * E + kCoopWarps * E) * sizeof(int);
+}
+
+// Largest grid a cooperative launch of the kernel can have (all blocks
+// resident), or 0 if the query fails.
+template <bool kScatter>
+int coop_capacity(size_t smem) {
+  auto kernel = layout_coop_kernel<kScatter>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kCoopThreads, smem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return per_sm * device_sm_count();
+}
+
+template <bool kScatter>
+int launch_coop(int grid, size_t smem, cudaStream_t s, const int32_t* ids, int64_t T, int K,
+                int E, int align, const int32_t* d_n_valid, int64_t M_cap, int nb,
+                int32_t* counts, unsigned* sync_words, int32_t* psum, int32_t* start,
+                int32_t* d_total, int32_t* tile_prefix, int32_t* m_indices, int32_t* src2dst,
+                int32_t* status, const CoopScatterArgs& sa) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kCoopThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, layout_coop_kernel<kScatter>, ids, T, K, E, align,
+                                           d_n_valid, M_cap, nb, counts, sync_words, psum, start,
+                                           d_total, tile_prefix, m_indices, src2dst, status, sa);
+  if (e != cudaSuccess) {
+    set_error("layout_coop_kernel: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  return check_launch("layout_coop_kernel");
+}
+
+}  // namespace
+}  // namespace moe
+
+namespace moe {
+namespace {
+
+// The layout of more than one chunk: one cooperative launch when the count
+// matrix fits in shared memory and every chunk's block can be resident at
+// once, else the count/scan launch and the rank launch. Both give the same
+// outputs bit for bit. sync_words: the zeroed 256-byte ticket slot.
+int layout_multi_chunk(const int32_t* ids, int64_t T, int K, int E, int align,
+                       const int32_t* d_n_valid, int64_t M_cap, int nb, int32_t* counts,
+                       int32_t* offs, unsigned* ticket, int32_t* psum, int32_t* start,
+                       int32_t* d_total, int32_t* tile_prefix, int32_t* m_indices,
+                       int32_t* src2dst, int32_t* d_status, cudaStream_t s) {
+  const size_t smem = coop_smem_bytes(E);
+  if (coop_capacity<false>(smem) >= nb) {
+    const CoopScatterArgs none = {};
+    return launch_coop<false>(nb, smem, s, ids, T, K, E, align, d_n_valid, M_cap, nb, counts,
+                              ticket, psum, start, d_total, tile_prefix, m_indices, src2dst,
+                              d_status, none);
+  }
+  layout_count_kernel<<<nb, kThreads, 0, s>>>(ids, T, K, E, align, d_n_valid, M_cap, nb, counts,
+                                              offs, ticket, psum, start, d_total, tile_prefix,
+                                              d_status);
+  int rc = check_launch("layout_count_kernel");
+  if (rc != MOE_OK) return rc;
+  layout_rank_kernel<<<nb, kThreads, 0, s>>>(ids, T, K, E, d_n_valid, M_cap, nb, offs, start,
+                                             d_total, m_indices, src2dst);
+  return check_launch("layout_rank_kernel");
+}
+
+}  // namespace
+}  // namespace moe
+
 extern "C" size_t moe_workspace_size(int64_t T, int K, int E) {
   if (T < 0 || K <= 0 || E <= 0) return 0;
   const int64_t nb = moe::num_chunks(T, K);
@@ -413,14 +910,9 @@ extern "C" int moe_expand_layout(const int32_t* topk_ids, int64_t T, int K, int 
                                                             m_indices, src2dst, d_status);
     return moe::check_launch("layout_single_kernel");
   }
-  moe::layout_count_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, align, d_n_valid, M_cap,
-                                                        nb, counts, offs, ticket, psum, start,
-                                                        d_total, tile_prefix, d_status);
-  int rc = moe::check_launch("layout_count_kernel");
-  if (rc != MOE_OK) return rc;
-  moe::layout_rank_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, d_n_valid, M_cap, nb,
-                                                       offs, start, d_total, m_indices, src2dst);
-  return moe::check_launch("layout_rank_kernel");
+  return moe::layout_multi_chunk(topk_ids, T, K, E, align, d_n_valid, M_cap, nb, counts, offs,
+                                 ticket, psum, start, d_total, tile_prefix, m_indices, src2dst,
+                                 d_status, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -545,195 +1037,27 @@ extern "C" int moe_expand_layout_noalloc(const int32_t* topk_ids, int64_t T, int
   int32_t* counts = static_cast<int32_t*>(ws);
   int32_t* offs = counts + static_cast<int64_t>(E) * nb;
   unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + need - 256);
-  // The array keeps whatever the previous call left; the ticket must start
-  // at zero (the counts and offsets are fully rewritten every call).
-  cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
+  // The array keeps whatever the previous call left; the ticket and the
+  // barrier words beside it must start at zero (the counts and offsets are
+  // fully rewritten every call).
+  cudaError_t e = cudaMemsetAsync(ticket, 0, moe::kSyncSlotBytes, s);
   if (e != cudaSuccess) {
     moe::set_error("moe_expand_layout_noalloc: cudaMemsetAsync: %s", cudaGetErrorString(e));
     return MOE_ERR_CUDA;
   }
-  moe::layout_count_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, align, d_n_valid, M_cap,
-                                                        nb, counts, offs, ticket, psum, start,
-                                                        d_total, tile_prefix, d_status);
-  rc = moe::check_launch("layout_count_kernel");
-  if (rc != MOE_OK) return rc;
-  moe::layout_rank_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, d_n_valid, M_cap, nb,
-                                                       offs, start, d_total, m_indices, src2dst);
-  return moe::check_launch("layout_rank_kernel");
+  return moe::layout_multi_chunk(topk_ids, T, K, E, align, d_n_valid, M_cap, nb, counts, offs,
+                                 ticket, psum, start, d_total, tile_prefix, m_indices, src2dst,
+                                 d_status, s);
 }
 
 // ---------------------------------------------------------------------------
 // moe_expand_layout_scatter: the layout fused into the scatter (SGLang PR
 // 37261 names layout and scatter as the two light/heavy halves of the expand
-// step; here they share launches). Launch 1 is layout_count_kernel above
-// (per-chunk histograms, last-block scan). Launch 2 replaces both the rank
-// pass and the stand-alone scatter: S blocks per 2048-pair chunk each rank
-// the whole chunk exactly as layout_rank_kernel does (the ranks only need the
-// chunk's base rows from launch 1, and redoing them costs a few KB of id
-// reads), keep the destinations in shared memory and copy their share of the
-// chunk's tokens: each token's fp8 row and scale row read once and stored to
-// its destinations, with the pair's weight. The first of the S blocks writes
-// src2dst; blocks placed first in the grid zero the alignment gaps; the chunk
-// blocks label m_indices. The outputs are those of moe_expand_layout followed
-// by moe_expand_scatter, bit for bit.
+// step). When the cooperative grid holds every chunk: layout_coop_kernel
+// <true>, one launch. Otherwise (one chunk, or more chunks than the grid
+// holds) moe_expand_layout followed by moe_expand_scatter. The outputs are
+// the same bit for bit either way.
 // ---------------------------------------------------------------------------
-namespace moe {
-namespace {
-
-constexpr int kPadRowsPerBlock = 8;
-
-__global__ void __launch_bounds__(kThreads) layout_rank_scatter_kernel(
-    const int32_t* __restrict__ ids, const float* __restrict__ topk_w,
-    const uint4* __restrict__ x, const void* __restrict__ x_scale, int ue8m0, int64_t ld_xs,
-    int64_t T, int H, int K, int E, int align, const int32_t* __restrict__ d_n_valid,
-    int64_t M_cap, int nb, int S, const int32_t* __restrict__ offs,
-    const int32_t* __restrict__ psum, const int32_t* __restrict__ start,
-    const int32_t* __restrict__ d_total, int32_t* __restrict__ m_indices,
-    int32_t* __restrict__ src2dst, uint4* __restrict__ xe, void* __restrict__ xe_scale,
-    int64_t ld_xes, float* __restrict__ row_w, int pad_blocks_per_expert) {
-  __shared__ int wcnt[kWarps * kMaxE];
-  __shared__ int s_start[kMaxE];
-  __shared__ int s_dst[kChunk];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nvec = H / 16;
-  const int G = H / 128;
-  const int W = (G + 3) / 4;
-  const int pad_blocks = E * pad_blocks_per_expert;
-
-  if (static_cast<int>(blockIdx.x) < pad_blocks) {
-    // zero rows [psum[e], align(psum[e])) of expert e, 8 rows per block
-    const int e = blockIdx.x / pad_blocks_per_expert;
-    const int sub = blockIdx.x % pad_blocks_per_expert;
-    const int64_t seg_end = align_up(psum[e], align);
-    const int64_t r0 = static_cast<int64_t>(psum[e]) + static_cast<int64_t>(sub) * kPadRowsPerBlock;
-    int64_t r1 = r0 + kPadRowsPerBlock;
-    if (r1 > seg_end) r1 = seg_end;
-    if (r1 > M_cap) r1 = M_cap;
-    for (int64_t r = r0; r < r1; ++r) {
-      for (int v = tid; v < nvec; v += kThreads) xe[r * nvec + v] = make_uint4(0, 0, 0, 0);
-      if (!ue8m0) {
-        for (int g = tid; g < G; g += kThreads) static_cast<float*>(xe_scale)[r * ld_xes + g] = 0.0f;
-      } else {
-        for (int j = tid; j < W; j += kThreads) static_cast<int32_t*>(xe_scale)[j * ld_xes + r] = 0;
-      }
-      if (tid == 0) row_w[r] = 0.0f;
-    }
-    return;
-  }
-
-  const int cb = blockIdx.x - pad_blocks;  // chunk block
-  const int chunk = cb / S;
-  const int part = cb % S;
-  for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
-  for (int e = tid; e < E; e += kThreads) s_start[e] = start[e];
-  __syncthreads();
-
-  // --- ranks: the rank pass of layout_rank_kernel for this chunk
-  const int64_t all_pairs = T * K;
-  const int64_t npairs = valid_rows(d_n_valid, T) * K;
-  const int64_t p0 = static_cast<int64_t>(chunk) * kChunk;
-  const int64_t base_p = p0 + warp * kPairsPerWarp;
-  int* my = wcnt + warp * E;
-  int idv[kRounds];
-#pragma unroll
-  for (int j = 0; j < kRounds; ++j) {
-    const int64_t p = base_p + j * 32 + lane;
-    idv[j] = (p < npairs) ? ids[p] : -1;
-  }
-#pragma unroll
-  for (int j = 0; j < kRounds; ++j)
-    if (idv[j] >= 0 && idv[j] < E) atomicAdd(&my[idv[j]], 1);
-  __syncthreads();
-  for (int e = tid; e < E; e += kThreads) {
-    int acc = offs[static_cast<int64_t>(e) * nb + chunk];
-    for (int w = 0; w < kWarps; ++w) {
-      const int c = wcnt[w * E + e];
-      wcnt[w * E + e] = acc;
-      acc += c;
-    }
-  }
-  __syncthreads();
-  const unsigned lt_mask = (1u << lane) - 1u;
-#pragma unroll
-  for (int j = 0; j < kRounds; ++j) {
-    const int64_t p = base_p + j * 32 + lane;
-    const int id = idv[j];
-    const bool valid = (id >= 0 && id < E);
-    const int key = valid ? id : (E + static_cast<int>(lane));
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    int dst = -1;
-    if (valid) dst = my[id] + __popc(peers & lt_mask);
-    __syncwarp();
-    if (valid && (peers & lt_mask) == 0u) my[id] += __popc(peers);
-    __syncwarp();
-    const int d = (dst >= 0 && dst < M_cap) ? dst : -1;
-    s_dst[warp * kPairsPerWarp + j * 32 + lane] = d;
-    if (part == 0 && p < all_pairs) src2dst[p] = d;
-  }
-  __syncthreads();
-
-  // --- copy: tokens of this chunk's valid pairs, every S-th one from `part`
-  int64_t p1 = p0 + kChunk;
-  if (p1 > npairs) p1 = npairs;
-  if (p1 > p0) {
-    const int64_t t_first = p0 / K;
-    const int64_t t_end = (p1 - 1) / K + 1;
-    for (int64_t t = t_first + part; t < t_end; t += S) {
-      const int64_t q0 = t * K;  // the token's first pair
-      const int k_lo = q0 < p0 ? static_cast<int>(p0 - q0) : 0;
-      const int k_hi = q0 + K > p1 ? static_cast<int>(p1 - q0) : K;
-      const int kb0 = static_cast<int>(q0 - p0);  // s_dst[kb0 + k]: pair k of token t
-      for (int v = tid; v < nvec; v += kThreads) {
-        const uint4 val = __ldcs(x + t * nvec + v);
-        for (int k = k_lo; k < k_hi; ++k) {
-          const int r = s_dst[kb0 + k];
-          if (r >= 0) xe[static_cast<int64_t>(r) * nvec + v] = val;
-        }
-      }
-      if (!ue8m0) {
-        const float* xs = static_cast<const float*>(x_scale);
-        for (int g = tid; g < G; g += kThreads) {
-          const float sv = xs[t * ld_xs + g];
-          for (int k = k_lo; k < k_hi; ++k) {
-            const int r = s_dst[kb0 + k];
-            if (r >= 0) static_cast<float*>(xe_scale)[static_cast<int64_t>(r) * ld_xes + g] = sv;
-          }
-        }
-      } else {
-        const int32_t* xs = static_cast<const int32_t*>(x_scale);
-        for (int j = tid; j < W; j += kThreads) {
-          const int32_t wv = xs[j * ld_xs + t];
-          for (int k = k_lo; k < k_hi; ++k) {
-            const int r = s_dst[kb0 + k];
-            if (r >= 0) static_cast<int32_t*>(xe_scale)[j * ld_xes + r] = wv;
-          }
-        }
-      }
-      if (tid >= k_lo && tid < k_hi && s_dst[kb0 + tid] >= 0) row_w[s_dst[kb0 + tid]] = topk_w[q0 + tid];
-    }
-  }
-
-  // --- row labels: e on [start[e], start[e] + align(count_e)), -1 past the total
-  const int total = *d_total;
-  const int64_t nchunk_blocks = static_cast<int64_t>(gridDim.x) - pad_blocks;
-  for (int64_t row = static_cast<int64_t>(cb) * kThreads + tid; row < M_cap;
-       row += nchunk_blocks * kThreads) {
-    int label = -1;
-    if (row < total) {
-      int lo = 0, hi = E - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_start[mid] <= row) lo = mid; else hi = mid - 1;
-      }
-      label = lo;
-    }
-    m_indices[row] = label;
-  }
-}
-
-}  // namespace
-}  // namespace moe
-
 extern "C" int moe_expand_layout_scatter(
     const int32_t* topk_ids, const float* topk_w, const uint8_t* x, const void* x_scale,
     int scale_layout, int64_t ld_xs, int64_t T, int H, int K, int E, int align,
@@ -773,28 +1097,44 @@ extern "C" int moe_expand_layout_scatter(
   }
   const int nb = static_cast<int>(moe::num_chunks(T, K));
   int32_t* counts = static_cast<int32_t*>(ws);
-  int32_t* offs = counts + static_cast<int64_t>(E) * nb;
   unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + need - 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  moe::layout_count_kernel<<<nb, moe::kThreads, 0, s>>>(topk_ids, T, K, E, align, d_n_valid, M_cap,
-                                                        nb, counts, offs, ticket, psum, start,
-                                                        d_total, tile_prefix, d_status);
-  int rc = moe::check_launch("layout_count_kernel");
-  if (rc != MOE_OK) return rc;
-  // S blocks per chunk: about four blocks per SM in all, and no more blocks
-  // per chunk than the chunk has tokens
-  int64_t tokens_per_chunk = (moe::kChunk + K - 1) / K + 1;
-  if (tokens_per_chunk > T + 1) tokens_per_chunk = T + 1;
-  int S = (4 * moe::device_sm_count() + nb - 1) / nb;
-  if (S > tokens_per_chunk) S = static_cast<int>(tokens_per_chunk);
-  if (S < 1) S = 1;
-  const int pad_per_expert = (align - 1 + moe::kPadRowsPerBlock - 1) / moe::kPadRowsPerBlock;
-  const int64_t grid = static_cast<int64_t>(E) * pad_per_expert + static_cast<int64_t>(nb) * S;
-  MOE_REQUIRE(grid < (1ll << 31), "moe_expand_layout_scatter: grid too large");
-  moe::layout_rank_scatter_kernel<<<static_cast<unsigned>(grid), moe::kThreads, 0, s>>>(
-      topk_ids, topk_w, reinterpret_cast<const uint4*>(x), x_scale,
-      scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR, ld_xs, T, H, K, E, align, d_n_valid, M_cap,
-      nb, S, offs, psum, start, d_total, m_indices, src2dst, reinterpret_cast<uint4*>(xe), xe_scale,
-      ld_xes, row_w, pad_per_expert);
-  return moe::check_launch("layout_rank_scatter_kernel");
+  auto layout_then_scatter = [&]() {
+    const int rc = moe_expand_layout(topk_ids, T, K, E, align, d_n_valid, M_cap, psum, start,
+                                     d_total, m_indices, src2dst, tile_prefix, ws, ws_bytes,
+                                     d_status, stream);
+    if (rc != MOE_OK) return rc;
+    return moe_expand_scatter(x, x_scale, scale_layout, ld_xs, topk_w, src2dst, psum, start,
+                              d_n_valid, T, H, K, E, align, M_cap, xe, xe_scale, ld_xes, row_w,
+                              d_status, stream);
+  };
+  // every pair in one chunk: the one-block layout, then the scatter
+  if (nb == 1) return layout_then_scatter();
+  if (K <= moe::kCoopMaxK) {
+    // one cooperative launch: layout, grid barrier, copy with the whole grid
+    const size_t smem = moe::coop_smem_bytes(E);
+    const int cap = moe::coop_capacity<true>(smem);
+    // the copy's work counter runs past the item count by at most one grab
+    // per warp and must stay inside 32 bits
+    const int64_t nseg = (H / 16 + moe::kCopyPiece - 1) / moe::kCopyPiece;
+    const int64_t counter_max =
+        T * nseg + static_cast<int64_t>(cap) * moe::kCoopWarps * moe::kCopyGrab;
+    if (cap >= nb && counter_max <= static_cast<int64_t>(UINT32_MAX)) {
+      moe::CoopScatterArgs sa;
+      sa.topk_w = topk_w;
+      sa.x = reinterpret_cast<const uint4*>(x);
+      sa.x_scale = x_scale;
+      sa.ue8m0 = scale_layout == MOE_SCALE_UE8M0_PACKED_COLMAJOR;
+      sa.ld_xs = ld_xs;
+      sa.H = H;
+      sa.xe = reinterpret_cast<uint4*>(xe);
+      sa.xe_scale = xe_scale;
+      sa.ld_xes = ld_xes;
+      sa.row_w = row_w;
+      return moe::launch_coop<true>(cap, smem, s, topk_ids, T, K, E, align, d_n_valid, M_cap, nb,
+                                    counts, ticket, psum, start, d_total, tile_prefix, m_indices,
+                                    src2dst, d_status, sa);
+    }
+  }
+  return layout_then_scatter();
 }

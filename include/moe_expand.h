@@ -106,6 +106,15 @@ size_t moe_workspace_size(int64_t T, int K, int E);
  *   tile_prefix int32 [E+1]   tile_prefix[e+1] - tile_prefix[e] =
  *                             ceil((align(psum[e]) - start[e]) / MOE_BLOCK_M)
  *   ws, ws_bytes  workspace of moe_workspace_size(T, K, E) bytes.
+ * Launches: one block when T*K <= 2048. Otherwise, when a cooperative grid
+ * (three 512-thread blocks per SM, fewer for very large E) holds one block
+ * per 2048-pair chunk, one launch: the blocks rank their chunk's pairs,
+ * publish their counts, meet at a grid-wide barrier, then each derives the
+ * offsets from the whole count table and writes its chunk's rows. The
+ * barrier wait is bounded; if it gives up the status word gets
+ * MOE_ERR_TIMEOUT and the outputs are not valid. More chunks take two
+ * launches (count and scan, then rank). All give the same outputs bit for
+ * bit.
  * Device errors: MOE_ERR_DEVICE_CHECK for an id >= E in a valid row (that
  * pair is skipped) or total > M_cap (rows past M_cap are not written).
  */
@@ -137,8 +146,8 @@ int moe_expand_layout(const int32_t* topk_ids, int64_t T, int K, int E, int alig
  *    whenever the current CUDA context of the device has changed (after a
  *    device reset); make that first call before any stream capture.
  *  - Every call shares the one array and it keeps the last call's contents;
- *    the call clears the part that must start at zero (an asynchronous 4-byte
- *    memset on the stream). Calls ordered on one stream may follow each other
+ *    the call clears the part that must start at zero (an asynchronous 8-byte
+ *    memset on the stream) and then launches what moe_expand_layout launches. Calls ordered on one stream may follow each other
  *    without a host wait. Calls that overlap on the GPU (different streams,
  *    no ordering between them) race on the array and give wrong results.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
@@ -151,16 +160,21 @@ int moe_expand_layout_noalloc(const int32_t* topk_ids, int64_t T, int K, int E, 
 
 /*
  * Layout fused into the expand-scatter (SGLang PR 37261: the layout kernels
- * and the expand copy of the do_expand=True dispatch, here in two launches
- * instead of three: the count/scan launch of moe_expand_layout, then one
- * launch that ranks each 2048-pair chunk and copies that chunk's rows).
+ * and the expand copy of the do_expand=True dispatch). For two or more
+ * 2048-pair chunks, when a cooperative grid of two 512-thread blocks per SM
+ * holds one block per chunk: ONE launch that runs the layout as
+ * moe_expand_layout does, meets at a second bounded grid-wide barrier, then
+ * labels m_indices, zeroes the gaps and copies every valid token's row with
+ * all its blocks. Otherwise (one chunk, or more chunks than that grid):
+ * moe_expand_layout followed by moe_expand_scatter.
  * Arguments: those of moe_expand_layout (topk_ids .. tile_prefix, the same
  * workspace of moe_workspace_size bytes, zeroed before its first use) plus
  * those of moe_expand_scatter (topk_w, x, x_scale/scale_layout/ld_xs, H, xe,
  * xe_scale/ld_xes, row_w). Every output equals, bit for bit, what
  * moe_expand_layout followed by moe_expand_scatter write. Asynchronous on
  * `stream`; the workspace must not be shared with a call that can overlap
- * this one. Errors: as the two calls it replaces.
+ * this one. Errors: as the two calls it replaces, plus MOE_ERR_TIMEOUT in the
+ * status word if a grid-wide barrier gives up (outputs then not valid).
  */
 int moe_expand_layout_scatter(const int32_t* topk_ids, const float* topk_w, const uint8_t* x,
                               const void* x_scale, int scale_layout, int64_t ld_xs, int64_t T,

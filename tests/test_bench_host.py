@@ -68,20 +68,43 @@ def test_reference_arm_other_ranks_do_nothing():
 
 
 def test_launches_per_step():
-    """The gpu_launches claim: kernels one step launches in each mode."""
+    """The gpu_launches claim: kernels one step launches in each mode, on a
+    152-SM GPU."""
     import argparse
     import bench
-    a = lambda **kw: argparse.Namespace(**{"fuse_layout_scatter": False, "masked_max_m": 0, **kw})  # noqa: E731
+    a = lambda **kw: argparse.Namespace(**{"fuse_layout_scatter": True, "masked_max_m": 0, **kw})  # noqa: E731
     big = synth.config_by_name("zipf_t16384_h7168")
     dec = synth.config_by_name("decode_t256_h7168_ue8m0")
-    # layout 2 + scatter + gate_up(+act+quant) + down + combine
-    assert bench.launches_per_step(a(), big, True) == 6
-    assert bench.launches_per_step(a(), big, False) == 7            # + stand-alone act_quant
-    assert bench.launches_per_step(a(masked_max_m=1152), big, True) == 8  # + two slab bridges
-    assert bench.launches_per_step(a(fuse_layout_scatter=True), big, True) == 5
-    # 256 x 8 pairs fit one 2048-pair chunk: the layout is one launch
-    assert bench.launches_per_step(a(), dec, True) == 5
-    assert bench.launches_per_step(a(fuse_layout_scatter=True), dec, True) == 5
+    pad = synth.config_by_name("padded_t32768_valid6000_h4096")
+    sms = 152
+    # fused layout+scatter (one cooperative launch) + gate_up(+act+quant) + down + combine
+    assert bench.launches_per_step(a(), big, True, sms) == 4
+    assert bench.launches_per_step(a(), pad, True, sms) == 4       # 128 chunks <= 2 x 152
+    assert bench.launches_per_step(a(), big, False, sms) == 5      # + stand-alone act_quant
+    assert bench.launches_per_step(a(masked_max_m=1152), big, True, sms) == 6  # + two slab bridges
+    # two calls: one cooperative layout launch + the scatter
+    assert bench.launches_per_step(a(fuse_layout_scatter=False), big, True, sms) == 5
+    # 256 x 8 pairs fit one 2048-pair chunk: one-block layout + scatter either way
+    assert bench.launches_per_step(a(), dec, True, sms) == 5
+    assert bench.launches_per_step(a(fuse_layout_scatter=False), dec, True, sms) == 5
+
+
+def test_front_launches_fall_back_past_the_cooperative_grid():
+    """More chunks than the cooperative grid holds: the fused call becomes
+    the two calls, and past three blocks per SM the layout takes two
+    launches."""
+    import bench
+    sms = 152
+    T, K, E, H = 2048 * 2 * sms // 8, 8, 32, 4096  # exactly 2 blocks per SM of chunks
+    assert bench.front_launches(T, K, E, H, True, sms) == 1
+    assert bench.front_launches(T + 256, K, E, H, True, sms) == 2   # layout coop + scatter
+    T3 = 2048 * 3 * sms // 8
+    assert bench.front_launches(T3, K, E, H, False, sms) == 2
+    assert bench.front_launches(T3 + 256, K, E, H, False, sms) == 3  # count + rank + scatter
+    assert bench.front_launches(T3 + 256, K, E, H, True, sms) == 3
+    # shared memory limits the blocks per SM for very many experts
+    assert bench.coop_blocks_per_sm(32, False) == 3 and bench.coop_blocks_per_sm(32, True) == 2
+    assert bench.coop_blocks_per_sm(1024, False) == 2
 
 
 def test_oracle_sample_on_a_thread_pool_matches_one_thread():

@@ -186,8 +186,21 @@ MULTI_CHUNK = (
 )
 
 
+# More chunks than the cooperative grids hold on a 152-SM GPU: 313 chunks
+# (past the fused kernel's two blocks per SM: the fused call becomes the
+# two calls) and 469 (past the layout kernel's three: the layout takes its
+# two-launch path).
+MANY_CHUNKS = (
+    synth.LayerConfig("chunks_313_k8", T=80000, H=128, I=128, E=8, K=8, align=16, seed=33,
+                      routing="zipf", zipf_s=1.1, zipf_zero_experts=1, inactive_frac=0.02),
+    synth.LayerConfig("chunks_469_k8_ue8m0", T=120000, H=128, I=128, E=8, K=8, align=32, seed=34,
+                      scale_mode=synth.SCALE_UE8M0, n_valid=119000, garbage_tail=True),
+)
+
+
 @pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
-@pytest.mark.parametrize("cfg", MULTI_CHUNK, ids=[c.name for c in MULTI_CHUNK])
+@pytest.mark.parametrize("cfg", MULTI_CHUNK + MANY_CHUNKS,
+                         ids=[c.name for c in MULTI_CHUNK + MANY_CHUNKS])
 def test_layout_scatter_multi_chunk_bit_exact(mx, orc, cfg, fused):
     """Layout and scatter over several chunks against the oracle, bit for
     bit, through moe_expand_layout + moe_expand_scatter and through
