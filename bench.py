@@ -42,16 +42,26 @@ WORKLOAD = synth.config_by_name("zipf_t16384_h7168")
 L2_FLUSH_BYTES = 256 << 20           # > the 126 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_PER_BF16 = 2.0                   # nominal dense fp8 : bf16 tensor rate
-# DRAM bytes (read + write) of one launch of the dominant kernel (gate_up with
-# act+quant in its epilogue) on the full workload, from one ncu capture of
-# this build:  python bench.py --workload W --steps 1 --warmup 3
-# --no-cpu-baseline --no-e2e, under ncu --metrics
-# dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
-# -k regex:grouped_gemm -s 6 -c 1. Update it whenever that kernel changes.
-GATE_UP_DRAM_BYTES = {
-    "zipf_t16384_h7168": 1776920064 + 261410304,
-    "ue8m0_t8192_h7168": 2579245056 + 142214912,
+# DRAM bytes (read + write) per algorithmic byte of the dominant kernel
+# (gate_up with act+quant in its epilogue), each from one ncu capture on a
+# workload that holds a few GB of device memory:
+#   python bench.py --workload W --steps 1 --warmup 3 --no-cpu-baseline
+#   --no-e2e --no-per-config --no-graph-extra --no-variants, under ncu
+#   --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+#   --clock-control none -k regex:grouped_gemm -s 6 -c 2
+# fp32 scales on uniform_t4096_h4096 (34816 expanded rows, 32 experts):
+# 549653760 + 51582208 bytes against 604962816 algorithmic; ue8m0 scales on
+# ue8m0_t2048_e16_h7168 (the ue8m0 workload's rows per expert, a quarter of
+# its experts; 17408 rows, 16 experts): 597162496 + 33378560 against
+# 631476224. A launch's traffic is reported as the ratio
+# times its own algorithmic bytes (gate_up_alg_bytes). Update whenever that
+# kernel changes.
+GATE_UP_DRAM_PER_ALG = {
+    "f32": (549653760 + 51582208) / 604962816,
+    "ue8m0": (597162496 + 33378560) / 631476224,
 }
+GATE_UP_DRAM_SOURCE = ("ncu dram__bytes_read+write per algorithmic byte on uniform_t4096_h4096 "
+                       "(fp32) / ue8m0_t2048_e16_h7168 (ue8m0), times this launch's bytes")
 
 
 def parse_args(argv=None):
@@ -81,6 +91,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-workload lines of the other four workloads")
     ap.add_argument("--per-config-steps", type=int, default=10)
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the variant lines (gather weighting, masked slab, decode batch, "
+                         "the layout and scatter as two calls)")
     ap.add_argument("--no-graph-extra", action="store_true",
                     help="skip the CUDA-graph replay timing added beside the eager step time")
     return ap.parse_args(argv)
@@ -189,6 +202,20 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gate_up_alg_bytes(cfg, M_pad: int, n_experts: int) -> int:
+    """Bytes the gate_up launch (act+quant in its epilogue) must move: the
+    expanded rows' codes and scales and the non-empty experts' W13 and its
+    128x128 block scales read; the fp8 intermediate and its scales written."""
+    H, I = cfg.H, cfg.I
+    GH, GI = H // 128, I // 128
+    if cfg.scale_mode == "f32":
+        a_s, o_s, w_s = 4 * GH, 4 * GI, 4
+    else:
+        a_s, o_s, w_s = 4 * ((GH + 3) // 4), 4 * ((GI + 3) // 4), 1
+    read = M_pad * (H + a_s) + n_experts * (2 * I * H + (2 * I // 128) * GH * w_s)
+    return read + M_pad * (I + o_s)
 
 
 def algorithmic_work(cfg, P: int, M_pad: int, nv: int):
@@ -368,6 +395,12 @@ def timed_steps(step, stream, steps: int, flush):
     return [ev[0].elapsed_time(ev[6]) for ev in evs], per_kernel
 
 
+def n_experts(layer) -> int:
+    """Experts with at least one row."""
+    lay = layer.lay
+    return int(((lay.psum - lay.start) > 0).sum().item())
+
+
 def layer_work(layer, cfg, nv):
     lay = layer.lay
     psum = lay.psum.cpu().numpy()
@@ -503,7 +536,9 @@ def run_ours(args, world, rank, local):
                     "kernel": "grouped_gemm (gate_up" + (" + act_quant epilogue)" if fused else ")"),
                     "achieved": kernels["gemm1"]["achieved"], "peak": round(fp8_peak, 1),
                     "unit": "TFLOP/s", "frac": kernels["gemm1"]["frac"],
-                    "traffic": GATE_UP_DRAM_BYTES.get(cfg.name) if fused else None,
+                    "traffic": (round(GATE_UP_DRAM_PER_ALG[cfg.scale_mode] * gate_up_alg_bytes(
+                        cfg, M_pad, n_experts(layer))) if fused else None),
+                    "traffic_source": GATE_UP_DRAM_SOURCE if fused else None,
                     "peak_source": f"{peak_src}: bf16 burst x {FP8_PER_BF16:g} (nominal fp8:bf16)"}
 
     result = {
@@ -542,6 +577,8 @@ def run_ours(args, world, rank, local):
         torch.cuda.empty_cache()
         result["per_config"] = run_per_config(args, mx, L, dev, stream, flush, hbm, fp8_peak,
                                               exclude=cfg.name)
+    if rank == 0 and not args.no_variants and not args.graph:
+        result["variants"] = run_variants(args, mx, L, dev, stream, flush, hbm, fp8_peak)
     return result, rank
 
 
@@ -579,6 +616,44 @@ def run_per_config(args, mx, L, dev, stream, flush, hbm, fp8_peak, exclude):
             "tokens_per_s": round(run["nv"] / (med / 1e3), 1), "steps": args.per_config_steps,
             "n_valid": run["nv"], "valid_pairs": P, "expanded_rows": M_pad, "scales": cfg.scale_mode,
             "kernels": kernel_split(per_kernel, work, run["fused"], args, hbm, fp8_peak)}
+        del run
+        torch.cuda.empty_cache()
+    return out
+
+
+# (name, workload, argument overrides, with a graph replay)
+VARIANTS = (
+    ("gather_weighting", "zipf_t16384_h7168", {"weighting": "gather"}, False),
+    ("layout_scatter_two_calls", "zipf_t16384_h7168", {"fuse_layout_scatter": False}, False),
+    ("masked_slab_1152", "uniform_t4096_h4096", {"masked_max_m": 1152}, False),
+    ("decode_batch", "decode_t256_h7168_ue8m0", {}, True),
+    ("decode_batch_masked_slab_64", "decode_t256_h7168_ue8m0", {"masked_max_m": 64}, False),
+)
+
+
+def run_variants(args, mx, L, dev, stream, flush, hbm, fp8_peak):
+    """The layer's variants, each on the workload it is meant for: median
+    step time and per-kernel split of `--per-config-steps` steps (plus a
+    CUDA-graph replay time for the decode batch)."""
+    import argparse
+    out = {}
+    for name, wl, over, graph in VARIANTS:
+        vargs = argparse.Namespace(**{**vars(args), **over})
+        cfg = synth.config_by_name(wl)
+        run = run_workload(vargs, mx, L, cfg, dev, stream, flush, args.per_config_steps)
+        steps, per_kernel = timed_steps(run["step"], stream, args.per_config_steps, flush)
+        if run["layer"].status.item() != 0:
+            raise RuntimeError(f"device status {run['layer'].status.item()} ({name})")
+        P, M_pad, work = layer_work(run["layer"], cfg, run["nv"])
+        med = statistics.median(steps)
+        out[name] = {"workload": wl, **{k: v for k, v in over.items()},
+                     "ms_per_step": round(med, 4), "tokens_per_s": round(run["nv"] / (med / 1e3), 1),
+                     "steps": args.per_config_steps,
+                     "kernels": kernel_split(per_kernel, work, run["fused"], vargs, hbm, fp8_peak)}
+        if graph:
+            gms = graph_replay_ms(run["layer"], run["d"], run["n_valid"], stream, flush,
+                                  max(10, args.per_config_steps))
+            out[name]["graph_replay_ms"] = round(gms, 4)
         del run
         torch.cuda.empty_cache()
     return out

@@ -192,15 +192,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int KB = p.Kd / BK;
   const int NB = p.N / 128;
 
-  auto tile_rows = [&](int tile, int& e, int& row0, int& rows) {
-    const int m = tile / num_n;
+  // Tiles go expert by expert. Inside an expert the fused gate_up goes n
+  // tile by n tile (the expert's m blocks for its first n tile, then for
+  // its second, ...): the CTAs that read one weight tile hold consecutive
+  // tile ids and run it at the same time, so an expert's W13 (29 MB at
+  // H = 7168, I = 2048) need not stay in L2 from one wave of tiles to the
+  // next; only its activation rows do. The down GEMM (W2 half that size,
+  // more n tiles) keeps the m-major order, which measured faster there.
+  auto tile_coords = [&](int tile, int& e, int& row0, int& rows, int& nt) {
     int lo = 0, hi = p.E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (s_tp[mid] <= m) lo = mid; else hi = mid - 1;
+      if (s_tp[mid] * num_n <= tile) lo = mid; else hi = mid - 1;
     }
     e = lo;
-    row0 = s_start[e] + (m - s_tp[e]) * BM;
+    const int j = tile - s_tp[e] * num_n;
+    int m_local;
+    if constexpr (kFused) {
+      const int mb = s_tp[e + 1] - s_tp[e];  // > 0: the expert owns the tile
+      nt = j / mb;
+      m_local = j - nt * mb;
+    } else {
+      m_local = j / num_n;
+      nt = j - m_local * num_n;
+    }
+    row0 = s_start[e] + m_local * BM;
     const int seg_end = (e + 1 < p.E) ? min(s_start[e + 1], total) : total;
     rows = min(BM, seg_end - row0);
   };
@@ -214,9 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       unsigned long long t_wait = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-        int e, row0, rows;
-        tile_rows(tile, e, row0, rows);
-        const int n0 = (tile % num_n) * BN;
+        int e, row0, rows, nt;
+        tile_coords(tile, e, row0, rows, nt);
+        const int n0 = nt * BN;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           const long long t0 = tracing ? clock64() : 0;
@@ -226,9 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
           tma_load_2d(sa, &tmA, kb * BK, row0, &full[stage]);
           if (kFused) {
-            const int t = tile % num_n;
-            tma_load_2d(sa + kABytes, &tmB, kb * BK, e * p.N + t * 128, &full[stage]);
-            tma_load_2d(sa + kABytes + kBBytes / 2, &tmB, kb * BK, e * p.N + I + t * 128,
+            tma_load_2d(sa + kABytes, &tmB, kb * BK, e * p.N + nt * 128, &full[stage]);
+            tma_load_2d(sa + kABytes + kBBytes / 2, &tmB, kb * BK, e * p.N + I + nt * 128,
                         &full[stage]);
           } else {
             tma_load_2d(sa + kABytes, &tmB, kb * BK, e * p.N + n0, &full[stage]);
@@ -314,11 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int slot = 0;
     uint32_t sphase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      int e, row0, rows;
-      tile_rows(tile, e, row0, rows);
+      int e, row0, rows, nt;
+      tile_coords(tile, e, row0, rows, nt);
       // weight-scale blocks of the B tile's two 128-row halves
-      const int nbh0 = kFused ? tile % num_n : (tile % num_n) * 2;
-      const int nbh1 = kFused ? I / 128 + tile % num_n : nbh0 + 1;
+      const int nbh0 = kFused ? nt : nt * 2;
+      const int nbh1 = kFused ? I / 128 + nt : nbh0 + 1;
       bool ok = true;
       for (int g = 0; g < KG; ++g) {
         const bool got = mbar_wait_warp(&sf_empty[slot], sphase ^ 1u, abort_flag, p.status);
@@ -367,8 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned long long t_ewait = 0, t_ework = 0;
     int iter = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++iter) {
-      int e, row0, rows;
-      tile_rows(tile, e, row0, rows);
+      int e, row0, rows, nt;
+      tile_coords(tile, e, row0, rows, nt);
       const long long t0 = tracing ? clock64() : 0;
       const int row_in_tile = quarter * 32 + lane;
       const int row = row0 + row_in_tile;
@@ -421,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t b;
         group_scale(amax, true, sc, inv, b);
         if (row_ok) {
-          const int t = tile % num_n;
+          const int t = nt;
           uint4* dst = reinterpret_cast<uint4*>(p.di + static_cast<int64_t>(row) * I + t * 128 +
                                                 half * 64);
 #pragma unroll
@@ -450,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (row_ok) {
-        const int col0 = (tile % num_n) * BN + half * 128;
+        const int col0 = nt * BN + half * 128;
         const float wm = p.row_w != nullptr ? p.row_w[row] : 1.0f;
         uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.N + col0);
         auto put = [&](const uint32_t (&v)[32], int q) {

@@ -97,6 +97,16 @@ EXTRA_CONFIGS = (
                 seed=20, routing="uniform", scale_mode=SCALE_UE8M0),
 )
 
+# Reduced copies of the ue8m0 workload for hardware-counter captures, which
+# belong on a few GB of device memory: the same hidden and intermediate
+# sizes, top-k and 1024 rows per expert (8 m blocks, so the GEMMs reuse an
+# expert's weights exactly as at full size), with a quarter of the experts
+# and of the tokens.
+PROFILE_CONFIGS = (
+    LayerConfig("ue8m0_t2048_e16_h7168", T=2048, H=7168, I=2048, E=16, K=8,
+                align=128, seed=3, routing="uniform", scale_mode=SCALE_UE8M0),
+)
+
 # Shapes small enough for the oracle to run every row in seconds, still
 # spanning several 128-row tiles, several N tiles and ragged tails.
 PARITY_CONFIGS = (
@@ -136,7 +146,7 @@ PARITY_CONFIGS = (
 
 
 def config_by_name(name: str) -> LayerConfig:
-    for c in CONFIGS + PARITY_CONFIGS + EXTRA_CONFIGS:
+    for c in CONFIGS + PARITY_CONFIGS + EXTRA_CONFIGS + PROFILE_CONFIGS:
         if c.name == name:
             return c
     raise KeyError(name)

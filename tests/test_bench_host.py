@@ -118,3 +118,20 @@ def test_oracle_sample_on_a_thread_pool_matches_one_thread():
     n2, _, y2 = bench._oracle_sample(cfg, d, 600.0, t_list=toks, threads=4)
     assert n1 == n2 == len(toks)
     assert all((y1[t] == y2[t]).all() for t in toks)
+
+
+def test_gate_up_traffic_ratio_inputs():
+    """The stored per-byte DRAM ratios divide by gate_up_alg_bytes of the
+    captured workloads (rows and experts as the layout gives them)."""
+    import bench
+    import oracle as orc
+    for name, scale in (("uniform_t4096_h4096", "f32"), ("ue8m0_t2048_e16_h7168", "ue8m0")):
+        cfg = synth.config_by_name(name)
+        inp = orc.to_numpy_inputs(synth.generate(cfg))
+        M_cap = orc.expanded_capacity(cfg.T * cfg.K, cfg.E, cfg.align)
+        rl = orc.layout(inp["topk_ids"], cfg.E, cfg.align, inp["n_valid"], M_cap)
+        ne = int(((rl["psum"] - rl["start"]) > 0).sum())
+        alg = bench.gate_up_alg_bytes(cfg, int(rl["total"]), ne)
+        assert cfg.scale_mode == scale
+        assert 0.98 < bench.GATE_UP_DRAM_PER_ALG[scale] < 1.02
+        assert alg in (604962816, 631476224)
