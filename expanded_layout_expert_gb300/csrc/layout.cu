@@ -5,16 +5,21 @@
 // labels rows from the device psum with no cumsum, no H2D copy and no
 // sentinel; the review thread fixes psum[i] = align(psum[i-1]) + count_i).
 //
-// Two launches, no spin-waits:
-//  1. count: each block histograms a 2048-pair chunk into the workspace; the
-//     last block to finish (atomic ticket, it never waits) scans the per-block
-//     counts into per-(expert, block) base rows and the per-expert aligned
-//     prefix, total and tile prefix.
-//  2. rank: each block re-reads its chunk in (token, k) order, warp by warp,
-//     and gives each valid pair base + rank (a stable counting sort); the
-//     same blocks label m_indices by binary search over the segment starts.
-// When every pair fits in one chunk (a decode-sized batch), one block does
-// both passes in a single launch and no workspace is touched.
+// Three forms, the same outputs bit for bit, all a stable counting sort of
+// the pairs in (token, k) order over 2048-pair chunks:
+//  - one chunk (a decode-sized batch): one block, one launch, no workspace;
+//  - several chunks that a cooperative grid holds: one launch of one block
+//    per chunk with a bounded grid-wide barrier between counting and
+//    ranking (layout_coop_kernel, below; fused with the expand-scatter it
+//    is also the scatter's launch);
+//  - more chunks: two launches without any wait.
+//     1. count: each block histograms its chunk into the workspace; the last
+//        block to finish (atomic ticket, it never waits) scans the per-block
+//        counts into per-(expert, block) base rows and the per-expert
+//        aligned prefix, total and tile prefix.
+//     2. rank: each block re-reads its chunk in (token, k) order, warp by
+//        warp, and gives each valid pair base + rank; the same blocks label
+//        m_indices by binary search over the segment starts.
 #include <mutex>
 
 #include "common.cuh"
