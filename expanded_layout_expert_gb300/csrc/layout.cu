@@ -20,6 +20,7 @@
 //     2. rank: each block re-reads its chunk in (token, k) order, warp by
 //        warp, and gives each valid pair base + rank; the same blocks label
 //        m_indices by binary search over the segment starts.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -797,9 +798,24 @@ size_t coop_smem_bytes(int E) {
 }
 
 // Largest grid a cooperative launch of the kernel can have (all blocks
-// resident), or 0 if the query fails.
+// resident), or 0 if the query fails. The answer for the last shared-memory
+// size asked is kept per device (the layer asks the same size every call)
+// when that size needs no function attribute (<= 48 KB, E <= 646), which a
+// new context would have lost.
 template <bool kScatter>
 int coop_capacity(size_t smem) {
+  constexpr int kDevices = 64;
+  static std::atomic<int64_t> cached[kDevices];  // smem << 32 | capacity, 0 = none
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const bool cacheable = dev >= 0 && dev < kDevices && smem <= 48 * 1024;
+  if (cacheable) {
+    const int64_t c = cached[dev].load(std::memory_order_relaxed);
+    if (c != 0 && static_cast<size_t>(c >> 32) == smem) return static_cast<int>(c & 0xFFFFFFFF);
+  }
   auto kernel = layout_coop_kernel<kScatter>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -813,7 +829,10 @@ int coop_capacity(size_t smem) {
     cudaGetLastError();
     return 0;
   }
-  return per_sm * device_sm_count();
+  const int cap = per_sm * device_sm_count();
+  if (cacheable && cap > 0)
+    cached[dev].store((static_cast<int64_t>(smem) << 32) | cap, std::memory_order_relaxed);
+  return cap;
 }
 
 template <bool kScatter>
