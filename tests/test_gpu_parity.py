@@ -591,14 +591,18 @@ def test_bounded_wait_times_out_and_the_context_survives(mx, cases):
     assert_final_close(u16(y)[:nv], c["ref"]["y"][:nv], "after timeout")
 
 
-def test_empty_and_all_inactive(mx):
-    E, K, T, H, I = 4, 2, 6, 256, 128
+@pytest.mark.parametrize("T", [6, 3000], ids=["one_chunk", "three_chunks"])
+def test_empty_and_all_inactive(mx, T):
+    """No valid pair (every id -1), then no valid row (n_valid = 0): on one
+    2048-pair chunk (the one-block layout) and on three (the cooperative
+    layout and the fused layout + scatter)."""
+    E, K, H, I = 4, 2, 256, 128
     dev = "cuda"
     ids = torch.full((T, K), -1, dtype=torch.int32, device=dev)
     lay = mx.expand_layout(ids, E, 32, 64)
     torch.cuda.synchronize()
     assert int(lay.total.item()) == 0 and (lay.m_indices == -1).all()
-    assert (lay.tile_prefix == 0).all()
+    assert (lay.tile_prefix == 0).all() and (lay.src2dst == -1).all()
     w13 = torch.zeros(E, 2 * I, H, dtype=torch.uint8, device=dev)
     s13 = torch.ones(E, 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
     w2 = torch.zeros(E, H, I, dtype=torch.uint8, device=dev)
@@ -618,6 +622,7 @@ def test_empty_and_all_inactive(mx):
     torch.cuda.synchronize()
     assert torch.isnan(y.float()).all()
     assert int(layer.lay.total.item()) == 0
+    assert (layer.lay.src2dst == -1).all() and layer.status.item() == 0
 
 
 @pytest.mark.parametrize("mode", ["expanded", "gather", "masked"])
