@@ -135,3 +135,13 @@ def test_gate_up_traffic_ratio_inputs():
         assert cfg.scale_mode == scale
         assert 0.98 < bench.GATE_UP_DRAM_PER_ALG[scale] < 1.02
         assert alg in (604962816, 631476224)
+
+
+def test_variant_lines_name_real_workloads_and_arguments():
+    """Every variant line runs a known workload with argument overrides the
+    bench parser defines."""
+    import bench
+    args = vars(bench.parse_args([]))
+    for name, workload, over, _graph in bench.VARIANTS:
+        synth.config_by_name(workload)
+        assert set(over) <= set(args), (name, over)
