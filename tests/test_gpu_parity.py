@@ -183,6 +183,10 @@ MULTI_CHUNK = (
                       scale_mode=synth.SCALE_UE8M0),
     synth.LayerConfig("chunks_k5_padded", T=1600, H=512, I=128, E=10, K=5, align=128, seed=32,
                       n_valid=900, garbage_tail=True),
+    # 1024 experts: the cooperative kernels' per-warp tables take 78 KB of
+    # shared memory and each lane of the expert scan walks 32 experts
+    synth.LayerConfig("chunks_e1024_k8", T=600, H=128, I=128, E=1024, K=8, align=16, seed=36,
+                      routing="uniform", inactive_frac=0.05),
 )
 
 
@@ -510,6 +514,44 @@ def test_device_checks_report_without_faulting(mx):
     assert int(lay.total.item()) == 32
     s2d = lay.src2dst.cpu().numpy()
     assert ((s2d == -1) | (s2d < 16)).all()
+
+
+def test_device_checks_on_several_chunks(mx):
+    """The same checks through the cooperative layout and the fused layout +
+    scatter (three 2048-pair chunks): an id >= E is flagged and its pair
+    dropped; a capacity below the aligned total is flagged, and nothing is
+    written at or past it."""
+    E, K, T, H = 8, 2, 3000, 128
+    g = torch.Generator().manual_seed(7)
+    ids = torch.randint(0, E, (T, K), generator=g, dtype=torch.int32).cuda()
+    ids[1234, 1] = E + 3
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M_cap = mx.expanded_capacity(T, K, E, 16)
+    lay = mx.expand_layout(ids, E, 16, M_cap, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == mx._capi.MOE_ERR_DEVICE_CHECK
+    assert lay.src2dst[1234, 1].item() == -1
+    assert int((lay.src2dst >= 0).sum().item()) == T * K - 1
+    # capacity below the total, through the fused call into guarded buffers
+    ids[1234, 1] = 0
+    small = 1024
+    x = torch.randint(0, 256, (T, H), dtype=torch.uint8, device="cuda")
+    xs = torch.ones(T, H // 128, dtype=torch.float32, device="cuda")
+    w = torch.rand(T, K, device="cuda")
+    xe = torch.full((small + 64, H), 0xAB, dtype=torch.uint8, device="cuda")
+    xe_s = torch.full((small + 64, H // 128), float("nan"), device="cuda")
+    rw = torch.full((small + 64,), float("nan"), device="cuda")
+    status.zero_()
+    lay, _, _, _ = mx.expand_layout_scatter(x, xs, mx.MOE_SCALE_F32_ROWMAJOR, ids, w, E, 16, small,
+                                            status=status, xe=xe[:small], xe_scale=xe_s[:small],
+                                            row_w=rw[:small])
+    torch.cuda.synchronize()
+    assert status.item() == mx._capi.MOE_ERR_DEVICE_CHECK
+    assert int(lay.total.item()) > small
+    s2d = lay.src2dst.cpu().numpy()
+    assert ((s2d == -1) | (s2d < small)).all()
+    assert (xe[small:] == 0xAB).all() and torch.isnan(rw[small:]).all()
+    assert torch.isnan(xe_s[small:]).all()
 
 
 @pytest.mark.parametrize("name", ["mid_f32", "mid_ue8m0_ragged", "wide_e160_k12"])
