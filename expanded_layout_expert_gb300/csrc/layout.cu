@@ -900,7 +900,7 @@ extern "C" size_t moe_workspace_size(int64_t T, int K, int E) {
   if (T < 0 || K <= 0 || E <= 0) return 0;
   const int64_t nb = moe::num_chunks(T, K);
   const size_t tables = static_cast<size_t>(2) * static_cast<size_t>(E) * nb * sizeof(int32_t);
-  return (tables + 255) / 256 * 256 + 256;  // + the ticket, in its own 256-byte slot
+  return 256 + (tables + 255) / 256 * 256;  // the ticket slot, then the tables
 }
 
 extern "C" int moe_expand_layout(const int32_t* topk_ids, int64_t T, int K, int E, int align,
@@ -922,9 +922,9 @@ extern "C" int moe_expand_layout(const int32_t* topk_ids, int64_t T, int K, int 
     return MOE_ERR_WORKSPACE;
   }
   const int nb = static_cast<int>(moe::num_chunks(T, K));
-  int32_t* counts = static_cast<int32_t*>(ws);
+  unsigned* ticket = static_cast<unsigned*>(ws);  // the first 256 bytes, whatever T is
+  int32_t* counts = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 256);
   int32_t* offs = counts + static_cast<int64_t>(E) * nb;
-  unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + need - 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (nb == 1) {
     // every pair in one chunk: one block, one launch, no workspace
@@ -1058,9 +1058,9 @@ extern "C" int moe_expand_layout_noalloc(const int32_t* topk_ids, int64_t T, int
   void* ws = nullptr;
   int rc = moe::noalloc_scratch(&ws);
   if (rc != MOE_OK) return rc;
-  int32_t* counts = static_cast<int32_t*>(ws);
+  unsigned* ticket = static_cast<unsigned*>(ws);  // the first 256 bytes, whatever T is
+  int32_t* counts = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 256);
   int32_t* offs = counts + static_cast<int64_t>(E) * nb;
-  unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + need - 256);
   // The array keeps whatever the previous call left; the ticket and the
   // barrier words beside it must start at zero (the counts and offsets are
   // fully rewritten every call).
@@ -1120,8 +1120,8 @@ extern "C" int moe_expand_layout_scatter(
     return MOE_ERR_WORKSPACE;
   }
   const int nb = static_cast<int>(moe::num_chunks(T, K));
-  int32_t* counts = static_cast<int32_t*>(ws);
-  unsigned* ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + need - 256);
+  unsigned* ticket = static_cast<unsigned*>(ws);  // the first 256 bytes, whatever T is
+  int32_t* counts = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   auto layout_then_scatter = [&]() {
     const int rc = moe_expand_layout(topk_ids, T, K, E, align, d_n_valid, M_cap, psum, start,

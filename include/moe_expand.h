@@ -81,11 +81,14 @@ typedef struct CUstream_st* moe_stream_t; /* the same type as cudaStream_t */
 int64_t moe_expanded_capacity(int64_t T, int K, int E, int align);
 
 /* Host. Bytes of device workspace moe_expand_layout needs for (T, K, E).
- * The workspace must be zero-filled once before its first use; every
- * successful call leaves it ready for the next call. It holds per-(expert,
- * 2048-pair chunk) counts and offsets and a completion ticket, so its size
- * depends on T*K and E only; unlike a workspace sized by the expanded
- * capacity, it takes no M_cap argument. */
+ * The workspace must be zero-filled once before its first use; every call
+ * leaves it ready for the next call. Its first 256 bytes hold the
+ * completion ticket and the cooperative launch's barrier words, at the same
+ * place for every (T, K, E), so one workspace sized for the largest call
+ * serves smaller ones too; then come per-(expert, 2048-pair chunk) counts
+ * and offsets, rewritten by every call. Its size depends on T*K and E only;
+ * unlike a workspace sized by the expanded capacity, it takes no M_cap
+ * argument. */
 size_t moe_workspace_size(int64_t T, int K, int E);
 
 /*
@@ -146,9 +149,10 @@ int moe_expand_layout(const int32_t* topk_ids, int64_t T, int K, int E, int alig
  *    whenever the current CUDA context of the device has changed (after a
  *    device reset); make that first call before any stream capture.
  *  - Every call shares the one array and it keeps the last call's contents;
- *    the call clears the part that must start at zero (an asynchronous 8-byte
- *    memset on the stream) and then launches what moe_expand_layout launches. Calls ordered on one stream may follow each other
- *    without a host wait. Calls that overlap on the GPU (different streams,
+ *    the call clears the part that must start at zero (an asynchronous
+ *    256-byte memset on the stream) and then launches what
+ *    moe_expand_layout launches. Calls ordered on one stream may follow
+ *    each other without a host wait. Calls that overlap on the GPU (different streams,
  *    no ordering between them) race on the array and give wrong results.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */

@@ -729,3 +729,27 @@ def test_host_pipeline_copies_only_the_valid_prefix(mx, cases, name):
         assert torch.equal(o[:nv], want)
         assert torch.isnan(o[nv:].float()).all()
     assert layer.status.item() == 0
+
+
+def test_one_workspace_serves_calls_of_different_sizes(mx, orc):
+    """A workspace sized for the largest call, reused by smaller ones in
+    between (three, one and 469 chunks: the cooperative layout, the one-block
+    layout, the two-launch layout): every result equals the oracle's, so the
+    barrier and ticket words the calls share start at zero every time."""
+    E, K, align = 8, 2, 16
+    sizes = (3000, 500, 480000, 3000, 700)
+    ws = torch.zeros(max(mx.workspace_size(T, K, E) for T in sizes), dtype=torch.uint8,
+                     device="cuda")
+    g = torch.Generator().manual_seed(9)
+    for T in sizes:
+        ids = torch.randint(-1, E, (T, K), generator=g, dtype=torch.int32)
+        M_cap = orc.expanded_capacity(T * K, E, align)
+        rl = orc.layout(ids.numpy(), E, align, T, M_cap)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        lay = mx.expand_layout(ids.cuda(), E, align, M_cap, ws=ws, status=status)
+        torch.cuda.synchronize()
+        assert status.item() == 0, T
+        assert int(lay.total.item()) == rl["total"], T
+        for k in ("psum", "start", "tile_prefix", "src2dst"):
+            assert np.array_equal(getattr(lay, k).cpu().numpy().reshape(-1),
+                                  np.asarray(rl[k]).reshape(-1)), (T, k)
