@@ -187,6 +187,12 @@ MULTI_CHUNK = (
     # shared memory and each lane of the expert scan walks 32 experts
     synth.LayerConfig("chunks_e1024_k8", T=600, H=128, I=128, E=1024, K=8, align=16, seed=36,
                       routing="uniform", inactive_frac=0.05),
+    # top-1 (one pair per token, lane 0 alone carries the rows in the copy)
+    # and top-32 (every lane of a copy warp holds a destination row)
+    synth.LayerConfig("chunks_k1", T=5000, H=256, I=128, E=8, K=1, align=32, seed=37,
+                      routing="zipf", zipf_s=1.1, zipf_zero_experts=2, inactive_frac=0.05),
+    synth.LayerConfig("chunks_k32_ue8m0", T=100, H=384, I=128, E=64, K=32, align=8, seed=38,
+                      routing="uniform", scale_mode=synth.SCALE_UE8M0),
 )
 
 
