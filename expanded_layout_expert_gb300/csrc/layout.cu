@@ -393,8 +393,8 @@ __global__ void __launch_bounds__(kThreads) layout_single_kernel(
 //   -- barrier of the chunk blocks --
 //   C. every chunk block reads the whole count table (E x chunks, from L2,
 //      a group of lanes per expert) and derives the expert totals, the
-//      aligned segment starts (one warp scans the experts) and its own
-//      chunk's first row per expert;
+//      aligned segment starts (one block-wide scan over the experts) and
+//      its own chunk's first row per expert;
 //   D. it writes src2dst of its chunk: segment start + earlier chunks +
 //      earlier warps + the rank inside the warp;
 //   E. the chunk blocks label m_indices, four consecutive rows per thread
@@ -460,6 +460,37 @@ MOE_DEV bool grid_sync(unsigned* arrivals, unsigned target, int32_t* status, int
   return *s_flag != 0;
 }
 
+// Exclusive scan of two ints per thread over the kCoopThreads threads:
+// {prefix of a, prefix of b, total of a, total of b}.
+MOE_DEV int4 coop_exclusive_scan2(int a, int b, int2* warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ia = a, ib = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ya = __shfl_up_sync(0xffffffffu, ia, o);
+    const int yb = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) {
+      ia += ya;
+      ib += yb;
+    }
+  }
+  if (lane == 31) warp_tot[warp] = make_int2(ia, ib);
+  __syncthreads();
+  int ba = 0, bb = 0, ta = 0, tb = 0;
+#pragma unroll
+  for (int w = 0; w < kCoopWarps; ++w) {
+    const int2 v = warp_tot[w];
+    if (w < warp) {
+      ba += v.x;
+      bb += v.y;
+    }
+    ta += v.x;
+    tb += v.y;
+  }
+  __syncthreads();
+  return make_int4(ba + ia - a, bb + ib - b, ta, tb);
+}
+
 // m_indices rows [r, r + 4) for r = first, first + stride, ...: e on
 // [start[e], start[e] + align(count_e)), -1 past the total; one search per
 // four rows.
@@ -515,6 +546,7 @@ __global__ void __launch_bounds__(kCoopThreads, kScatter ? 2 : 3) layout_coop_ke
   int* s_start = hist + E;         // [E] segment starts
   int* s_base = s_start + E;       // [E] this chunk's first row per expert
   int* wcnt = s_base + E;          // [kCoopWarps][E] per-warp counts, then offsets
+  __shared__ int2 warp_tot[kCoopWarps];
   __shared__ int s_flag, s_total;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = static_cast<int>(blockIdx.x);
@@ -601,30 +633,19 @@ __global__ void __launch_bounds__(kCoopThreads, kScatter ? 2 : 3) layout_coop_ke
         }
       }
       __syncthreads();
-      // segment starts and tile prefix: warp 0 scans the experts, each lane
-      // a contiguous run of them
-      if (warp == 0) {
-        const int per = (E + 31) / 32;
-        const int e_lo = min(E, lane * per), e_hi = min(E, e_lo + per);
+      // segment starts and tile prefix: one scan over the experts of
+      // (aligned rows, tiles), every thread a contiguous run of experts
+      {
+        const int per = (E + kCoopThreads - 1) / kCoopThreads;
+        const int e_lo = min(E, tid * per), e_hi = min(E, e_lo + per);
         int rows = 0, tiles = 0;
         for (int e = e_lo; e < e_hi; ++e) {
           const int seg = align_up(hist[e], align);
           rows += seg;
           tiles += (seg + MOE_BLOCK_M - 1) / MOE_BLOCK_M;
         }
-        int ir = rows, it = tiles;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int yr = __shfl_up_sync(0xffffffffu, ir, o);
-          const int yt = __shfl_up_sync(0xffffffffu, it, o);
-          if (lane >= o) {
-            ir += yr;
-            it += yt;
-          }
-        }
-        const int rows_total = __shfl_sync(0xffffffffu, ir, 31);
-        const int tiles_total = __shfl_sync(0xffffffffu, it, 31);
-        int run = ir - rows, trun = it - tiles;
+        const int4 sc = coop_exclusive_scan2(rows, tiles, warp_tot);
+        int run = sc.x, trun = sc.y;
         for (int e = e_lo; e < e_hi; ++e) {
           const int c = hist[e];
           const int seg = align_up(c, align);
@@ -638,12 +659,12 @@ __global__ void __launch_bounds__(kCoopThreads, kScatter ? 2 : 3) layout_coop_ke
           run += seg;
           trun += (seg + MOE_BLOCK_M - 1) / MOE_BLOCK_M;
         }
-        if (lane == 0) {
-          s_total = rows_total;
+        if (tid == 0) {
+          s_total = sc.z;
           if (b == 0) {
-            tile_prefix[E] = tiles_total;
-            *d_total = rows_total;
-            if (rows_total > M_cap) set_status(status, MOE_ERR_DEVICE_CHECK);
+            tile_prefix[E] = sc.w;
+            *d_total = sc.z;
+            if (sc.z > M_cap) set_status(status, MOE_ERR_DEVICE_CHECK);
           }
         }
       }
